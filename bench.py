@@ -1,0 +1,369 @@
+"""Benchmark of the paged-attention hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch: append the new
+tokens' K/V (pa_reshape_and_cache), decode one token per sequence (pa_decode:
+split-K partitions plus the reduce), and the chunked-prefill requests when the
+workload has any (pa_prefill_chunk).  The default workload is the Llama-3-8B
+shaped decode batch: 256 sequences, 32 query / 8 KV heads, head_dim 128,
+16-token blocks, lengths U[512, 4096], bf16 — about 2.4 GB of K/V per step,
+far more than the 129 MB L2, so no flush is needed between steps.
+
+Metric: unique K/V bytes the decode must read per step / step time, in GB/s,
+plus decode tokens/s and steps/s.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU fp64 oracle, timed on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode tokens/s"
+DEFAULT_WORKLOAD = "llama3-8b-bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+# ncu DRAM traffic of the main decode kernel on this workload, per launch
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
+# source is byte-identical to what was profiled (sha256 of csrc/decode.cu).
+NCU_TRAFFIC = {}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _src_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "paged_kv_cache_25_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- reference arm
+def oracle_sample(wl_name: str, n_seqs: int | None, target_s: float, seed_offset: int = 0):
+    """Times the CPU oracle on a bounded sample of the workload's decode batch.
+    Returns (GB/s, seconds per sample, sample description, threads)."""
+    import oracle
+    from paged_kv_cache_25_gb300 import inputs
+    wl = inputs.get(wl_name)
+    dr = inputs.Draws(wl, wl.seed + seed_offset)
+    lens, sharers = dr.decode_lens(), dr.sharers()
+    prefix = dr.prefix_kv() if sharers.any() else None
+    q_all = dr.q()
+    threads = oracle.default_threads()
+    row = 2 * wl.n_kv_heads * wl.head_dim * wl.elem_bytes
+
+    def run(seqs):
+        ks, vs = [], []
+        for s in seqs:
+            k, v = dr.seq_kv(s, int(lens[s]), bool(sharers[s]), prefix)
+            ks.append(k); vs.append(v)
+        t0 = time.perf_counter()
+        oracle.decode(q_all[seqs], ks, vs, wl.scale, threads=threads)
+        return time.perf_counter() - t0
+
+    if n_seqs is None:
+        probe = list(range(min(2, wl.batch)))
+        t = run(probe)
+        per_tok = t / max(1, int(lens[probe].sum()))
+        want = target_s / max(per_tok, 1e-9)
+        n, acc = 0, 0
+        while n < wl.batch and acc < want:
+            acc += int(lens[n]); n += 1
+        n_seqs = max(1, n)
+    seqs = list(range(n_seqs))
+    t = run(seqs)
+    kv = int(lens[seqs].sum()) * row
+    desc = (f"first {n_seqs} of {wl.batch} decode sequences ({int(lens[seqs].sum())} of "
+            f"{int(lens.sum())} tokens), fp64 oracle incl. its fp64 packing, {threads} threads")
+    return kv / t / 1e9, t, desc, threads, n_seqs
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from paged_kv_cache_25_gb300 import inputs
+    wl = inputs.get(args.workload)
+    # size each step's sample so W + K steps take a few minutes at most
+    _, t_probe, _, threads, n = oracle_sample(args.workload, None, 2.0)
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, n, 0)
+    vals, times = [], []
+    desc = ""
+    for _ in range(args.steps):
+        v, t, desc, threads, _ = oracle_sample(args.workload, n, 0)
+        vals.append(v); times.append(t)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "n_q_heads": wl.n_q_heads,
+                   "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "sample_seqs": n},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from paged_kv_cache_25_gb300 import binding as pa
+    from paged_kv_cache_25_gb300 import build as pa_build
+    from paged_kv_cache_25_gb300 import inputs
+    from paged_kv_cache_25_gb300.step import PagedStep
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(pa_build.LIB):
+        pa_build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    pa.lib()
+    wl = inputs.get(args.workload)
+    st = PagedStep(wl, seed=wl.seed + rank, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    assert pa.pa_get_device_error() == 0
+
+    launches_per_step = 2 + (1 if st.workspace is not None else 0) + (1 if st.R else 0)
+    for _ in range(max(args.warmup, 3)):
+        st.step()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-timed region: inputs resident in HBM ---------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:            # torch creates the CUDA event at its first record
+        a.record(stream)
+        b.record(stream)
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    phys = int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].strip().isdigit() else local_rank
+    clocks = ClockSampler(phys)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)   # let the sampler start before the timed region
+    t_start.record(stream)
+    for i in range(args.steps):
+        pa.pa_set_profile_events(*ev[i])
+        st.step()
+    t_stop.record(stream)
+    torch.cuda.synchronize(dev)
+    pa.pa_set_profile_events(None, None)
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    assert pa.pa_get_device_error() == 0
+    ms_total = t_start.elapsed_time(t_stop)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # ---- end to end through the public API with host buffers --------------
+    B = wl.batch
+    pin = {
+        "q": st.q.cpu().pin_memory(), "k": st.new_k.cpu().pin_memory(),
+        "v": st.new_v.cpu().pin_memory(), "slots": st.new_slots.cpu().pin_memory(),
+        "bt": st.block_tables.cpu().pin_memory(), "cl": st.context_lens.cpu().pin_memory(),
+    }
+    if st.R:
+        pin.update({"pq": st.p_q_dev.cpu().pin_memory(), "qsl": st.query_start_loc.cpu().pin_memory(),
+                    "pbt": st.p_block_tables.cpu().pin_memory(),
+                    "pcl": st.p_context_lens.cpu().pin_memory()})
+    dst = {"q": st.q, "k": st.new_k, "v": st.new_v, "slots": st.new_slots, "bt": st.block_tables,
+           "cl": st.context_lens}
+    if st.R:
+        dst.update({"pq": st.p_q_dev, "qsl": st.query_start_loc, "pbt": st.p_block_tables,
+                    "pcl": st.p_context_lens})
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    pout_host = torch.empty(st.p_out.shape, dtype=st.p_out.dtype).pin_memory() if st.R else None
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_host.numel() * out_host.element_size() + (
+        pout_host.numel() * pout_host.element_size() if st.R else 0)
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step():
+        for k_, t in pin.items():
+            dst[k_].copy_(t, non_blocking=True)
+        st.step()
+        out_host.copy_(st.out, non_blocking=True)
+        if st.R:
+            pout_host.copy_(st.p_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # ---- reductions over ranks (max time) --------------------------------
+    ms_step = ms_total / args.steps
+    dec_ms = statistics.mean(decode_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step, e2e_ms, dec_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms, dec_ms = (float(x) for x in t.tolist())
+
+    kv_unique = st.kv_bytes_unique()
+    kv_logical = st.kv_bytes_logical()
+    value = world * kv_unique / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    # algorithmic bytes of the main decode kernel per launch: the unique K/V
+    # bytes plus q, the output/partials are < 0.5% and not counted
+    achieved = kv_unique / (dec_ms * 1e-3) / 1e9
+    src = _src_hash("decode.cu")
+    tr = NCU_TRAFFIC.get((wl.name, src))
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"torch.bfloat16": "bf16", "torch.float16": "f16", "torch.float32": "f32"}[str(wl.dtype)],
+        "data": "synthetic (seeded N(0,1) K/V/Q, random block scatter)",
+        "config": {"workload": wl.name, "batch": B, "n_q_heads": wl.n_q_heads,
+                   "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "num_blocks": st.num_blocks,
+                   "prefill_requests": st.R, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({kv_unique / 1e9:.2f} GB of K/V per step); no flush"},
+        "decode_tokens_per_s": world * B / (ms_step * 1e-3),
+        "steps_per_s": 1e3 / ms_step,
+        "pct_of_hbm_peak": 100.0 * value / world / peak,
+        "kv_bytes_unique_per_step": kv_unique, "kv_bytes_logical_per_step": kv_logical,
+        "decode_kernel_ms": dec_ms,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": tr,
+                     "kernel": "decode_mma_kernel", "peak_source": f"hbm_gbs ({peak_kind})"},
+        "e2e": {"value": world * kv_unique / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if st.R:
+        line["prefill_flops_per_step"] = st.prefill_flops()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, t, desc, threads, _ = oracle_sample(wl.name, None, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": desc, "seconds": t}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

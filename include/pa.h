@@ -1,0 +1,210 @@
+/*
+ * pa.h - C ABI of the GB300 paged-attention library (libpa.so).
+ *
+ * The operations follow the pages' statement of the problem:
+ *   "vLLM Serving - PagedAttention, Continuous Batching, and Production
+ *   Tuning", sections "PagedAttention in depth" (fixed-size KV blocks in one
+ *   pool, a per-sequence block table mapping logical to physical blocks) and
+ *   "How the attention kernel actually reads paged blocks" (the kernel takes
+ *   the block table as input, looks a block up once per block, computes q.k
+ *   against the keys of that block and accumulates the softmax-weighted sum of
+ *   the values of the same block);
+ *   "Life of a prompt", section "Back to the queue, and into vLLM proper"
+ *   (each decode step appends one K and one V row into the next free slot, a
+ *   fresh block every block_size tokens, a FIFO free-block queue);
+ *   "The hands-on guide to LLM Inference with vLLM", chunked prefill (each
+ *   chunk attends over every earlier cached token plus itself).
+ *
+ * Conventions for every call below:
+ *   - Device pointers are owned by the caller; the library allocates nothing
+ *     on the device.  Scratch space ("workspace") is passed in by the caller and
+ *     sized with the *_workspace_size queries.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All device work is enqueued asynchronously on it.
+ *   - Argument checks happen on the host before any launch.  A failed check
+ *     returns a status other than PA_OK and launches nothing;
+ *     pa_last_error_message() then describes it.
+ *   - Data errors only visible on the device (a block id outside [0,
+ *     num_blocks), a slot beyond the pool) set a sticky device error word and
+ *     skip the affected unit of work (its outputs are then unspecified).  No
+ *     kernel traps or asserts.  Read and clear the word with
+ *     pa_get_device_error().
+ *   - Every wait inside a kernel is bounded in time; a wait that runs out sets
+ *     PA_ERR_TIMEOUT in the device error word and the kernel returns.
+ *
+ * KV cache layout (one transformer layer, K and V in separate tensors):
+ *   k_cache, v_cache : [num_blocks][n_kv_heads][block_size][head_dim], row-major.
+ *   The token at logical position p of sequence s lives in physical block
+ *   block_tables[s][p / block_size], row p % block_size.  Its slot number is
+ *   physical_block * block_size + p % block_size.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* a pointer, size or shape check failed          */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim, block size) */
+    PA_ERR_OUT_OF_RANGE = 3,  /* device: block id or slot outside the pool       */
+    PA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required      */
+    PA_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out                  */
+    PA_ERR_CUDA = 6           /* a CUDA runtime call failed                      */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Shape of one layer's paged K/V pool.  head_dim in {64, 128} and block_size
+ * in {16, 32} run on the tensor-core paths; fp32 pools run on a CUDA-core
+ * path.  n_kv_heads >= 1. */
+typedef struct {
+    int num_blocks;
+    int block_size;
+    int n_kv_heads;
+    int head_dim;
+    pa_dtype dtype;
+} pa_cache_desc;
+
+/* ---------------------------------------------------------------- cache write
+ * Append K/V rows into their slots ("Life of a prompt": one new K and V
+ * vector per token go into the next free slot of the sequence's blocks).
+ *   k, v          : [num_tokens][n_kv_heads][head_dim], contiguous, cache dtype.
+ *   k_cache/v_cache: pools as in the layout above; written in place.
+ *   slot_mapping  : int64 [num_tokens] on the device.  slot < 0 means "skip this
+ *                   token" (padding).  slot >= num_blocks*block_size sets
+ *                   PA_ERR_OUT_OF_RANGE on the device and the token is skipped.
+ *                   Two tokens with one slot: the winner is unspecified.
+ * Only the addressed rows of the pools change, bit for bit.  Pointers must be
+ * 16-byte aligned.  num_tokens == 0 is a no-op. */
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int num_tokens,
+                               const pa_cache_desc* cache, void* stream);
+
+/* ---------------------------------------------------------------- decode
+ * One query row per sequence ("Life of a prompt", "The decode stage"):
+ *   out[s][h] = softmax(scale * q[s][h] . K_s^T) V_s
+ * over the context_lens[s] logical rows of sequence s, read through its block
+ * table ("How the attention kernel actually reads paged blocks").  Query head
+ * h reads KV head h / (n_q_heads / n_kv_heads) (grouped-query attention).
+ *   out          : [num_seqs][n_q_heads][head_dim] in out_dtype.
+ *   q            : [num_seqs][n_q_heads][head_dim], cache dtype.
+ *   block_tables : int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                  ceil(len / block_size) are never read.
+ *   context_lens : int32 [num_seqs]; the count includes the newest token
+ *                  (append it with pa_reshape_and_cache first).  Each must be in
+ *                  [1, max_blocks_per_seq * block_size]: the host cannot check
+ *                  device values, so a length outside that range is a caller
+ *                  error (rows past the table are clamped away; length 0 gives
+ *                  undefined output for that sequence).
+ *   block_size   : must equal cache->block_size.
+ *   workspace    : device scratch of at least pa_decode_workspace_size(...)
+ *                  bytes for the same shapes, 256-byte aligned; NULL allowed
+ *                  when that size is 0.  Long contexts are split over several
+ *                  thread blocks and combined by a second kernel through it.
+ * n_q_heads must be a multiple of n_kv_heads.  Accumulation is fp32. */
+pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
+                    const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int num_seqs, int n_q_heads,
+                    float scale, int block_size,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace pa_decode needs for sequences of at most max_context_len
+ * tokens (0 when no sequence is long enough to be split). */
+size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
+                                int block_size, int max_context_len);
+
+/* ---------------------------------------------------------------- chunked prefill
+ * A chunk of C_r new query rows of request r attends causally over the paged
+ * context ("The hands-on guide ...", chunked prefill): query row i sits at
+ * absolute position context_lens[r] - C_r + i and attends logical rows
+ * 0 .. that position.  The chunk's own K/V must already be in the pool
+ * (pa_reshape_and_cache).  With no earlier context it is ordinary causal
+ * prefill of the whole prompt.
+ *   out, q          : [total_q][n_q_heads][head_dim], request r's rows start at
+ *                     query_start_loc[r]; out in out_dtype, q in cache dtype.
+ *   query_start_loc : int32 [num_reqs + 1] on the device, non-decreasing,
+ *                     query_start_loc[0] = 0; C_r = difference of neighbours.
+ *   context_lens    : int32 [num_reqs] on the device: total tokens L_r of
+ *                     request r including the chunk (C_r <= L_r).
+ *   max_query_len   : host value >= every C_r (sizes the grid).
+ *   workspace       : reserved; pass NULL / 0 (pa_prefill_workspace_size is 0).
+ * bf16 and fp16 pools only. */
+pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q,
+                           const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* query_start_loc, const int32_t* context_lens,
+                           int num_reqs, int max_query_len, int n_q_heads,
+                           float scale, int block_size,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+size_t pa_prefill_workspace_size(int num_reqs, int n_q_heads, int head_dim, int total_q);
+
+/* ---------------------------------------------------------------- errors
+ * Synchronizes `stream`, returns the device error word (PA_OK if clean) and
+ * clears it.  The word is per device and shared by every stream. */
+pa_status pa_get_device_error(void* stream);
+const char* pa_status_string(pa_status status);
+/* Text of the last host-side failure on the calling thread ("" if none). */
+const char* pa_last_error_message(void);
+
+/* Measurement hook: when both are non-NULL, pa_decode records `start` right
+ * before its main attention kernel and `stop` right after it on the call's
+ * stream (cudaEvent_t passed as void*).  Pass NULL, NULL to turn it off. */
+void pa_set_profile_events(void* start, void* stop);
+
+/* ---------------------------------------------------------------- host allocator
+ * The free-block queue and page tables of "Life of a prompt" ("Back to the
+ * queue, and into vLLM proper"): a FIFO queue of free physical block ids, a
+ * reference count per block for sharing ("Sharing and copy-on-write"), blocks
+ * returned to the tail of the queue the moment their count reaches zero.
+ * Host memory only; not thread-safe (one owner thread). */
+typedef struct pa_alloc pa_alloc;
+/* initial_order: the queue's starting order (a permutation of 0..n-1), or NULL
+ * for 0..n-1.  Returns NULL on bad arguments. */
+pa_alloc* pa_alloc_create(int num_blocks, const int32_t* initial_order);
+/* Takes n blocks from the head of the queue into out (refcount 1 each).
+ * Returns 0, or -1 (nothing taken) if fewer than n are free. */
+int  pa_alloc_blocks(pa_alloc* a, int n, int32_t* out);
+/* Adds one reference to each listed block (another table points at it). */
+void pa_alloc_share(pa_alloc* a, const int32_t* ids, int n);
+/* Drops one reference from each listed block; a block reaching zero goes back
+ * to the tail of the queue. */
+void pa_alloc_free(pa_alloc* a, const int32_t* ids, int n);
+int  pa_alloc_num_free(const pa_alloc* a);
+int  pa_alloc_refcount(const pa_alloc* a, int block_id);
+void pa_alloc_destroy(pa_alloc* a);
+
+/* Builds block tables for a batch, sequences in order, ceil(len/block_size)
+ * blocks each.  Sequences flagged in `sharer` (may be NULL) point their first
+ * prefix_tokens/block_size entries at one set of prefix blocks taken once,
+ * before any sequence, and shared (refcount = number of sharers);
+ * prefix_tokens must be a multiple of block_size.  Unused entries are -1.
+ * tables: int32 [num_seqs][max_blocks_per_seq] host memory. */
+pa_status pa_alloc_build_tables(pa_alloc* a, int num_seqs, const int32_t* lens,
+                                const uint8_t* sharer, int prefix_tokens, int block_size,
+                                int max_blocks_per_seq, int32_t* tables);
+
+/* Host: slots[t] = tables[seq[t]][pos[t] / block_size] * block_size
+ *                  + pos[t] % block_size.  Returns PA_ERR_INVALID_ARG if a
+ * position falls outside the table or on an unused (-1) entry. */
+pa_status pa_slot_mapping(const int32_t* tables, int max_blocks_per_seq, int block_size,
+                          const int32_t* seq, const int32_t* pos, int num_tokens,
+                          int64_t* slots);
+
+/* Sizing ("vLLM Serving ...", "How big is the KV cache?"):
+ * 2 * n_layers * n_kv_heads * head_dim * elem_bytes, and the number of whole
+ * blocks of block_size tokens that fit in pool_bytes. */
+int64_t pa_kv_bytes_per_token(int n_layers, int n_kv_heads, int head_dim, int elem_bytes);
+int64_t pa_pool_blocks(int64_t pool_bytes, int block_size, int64_t bytes_per_token);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

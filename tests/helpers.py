@@ -1,0 +1,52 @@
+"""Shared test helpers: expected values come from the oracle fed by the seeded
+generator only (never from the CUDA path)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_25_gb300 import inputs
+
+# max |error| bars: fp32 inputs 1e-5; bf16/fp16 inputs 2e-3 (fp32 accumulation)
+TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-3, torch.float16: 2e-3}
+
+
+def half_ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """Half a unit in the last place of |x| in dtype: the rounding of the store."""
+    mant = {torch.bfloat16: 8, torch.float16: 11, torch.float32: 24}[dtype]
+    ax = np.maximum(np.abs(x), {torch.float16: 6.1e-5, torch.bfloat16: 1e-30,
+                                torch.float32: 1e-30}[dtype])
+    e = np.floor(np.log2(ax))
+    return 0.5 * np.exp2(e - (mant - 1))
+
+
+def oracle_decode(step, seqs=None, threads=None) -> np.ndarray:
+    """fp64 decode for the given decode sequences of a PagedStep's workload."""
+    dr, wl = step.draws, step.wl
+    seqs = list(range(wl.batch)) if seqs is None else list(seqs)
+    prefix = dr.prefix_kv() if step.prefix else None
+    ks, vs = [], []
+    for s in seqs:
+        k, v = dr.seq_kv(s, int(step.lens[s]), bool(step.sharers[s]), prefix)
+        ks.append(k); vs.append(v)
+    q = dr.q()[seqs]
+    return oracle.decode(q, ks, vs, wl.scale, threads=threads)
+
+
+def oracle_prefill_rows(step, r: int, rows, threads=None) -> np.ndarray:
+    """fp64 outputs of chosen query rows of prefill request r: row i attends
+    keys 0..L-C+i, i.e. a decode over the truncated logical K/V."""
+    dr, wl = step.draws, step.wl
+    L, C = int(step.p_lens[r]), int(step.p_chunk[r])
+    k, v = dr.prefill_kv(r, L)
+    q = dr.prefill_q(r)
+    outs = []
+    for i in rows:
+        p = L - C + i
+        outs.append(oracle.decode(q[i:i + 1], [k[:p + 1]], [v[:p + 1]], wl.scale, threads=threads)[0])
+    return np.stack(outs)
+
+
+def max_err(got: torch.Tensor, ref: np.ndarray) -> float:
+    return float(np.max(np.abs(got.detach().float().cpu().numpy().astype(np.float64) - ref)))

@@ -1,0 +1,101 @@
+"""GPU parity of chunked prefill over paged context against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_25_gb300 import binding as pa
+from paged_kv_cache_25_gb300 import inputs
+from paged_kv_cache_25_gb300.step import PagedStep
+from tests.helpers import TOL, half_ulp, max_err, oracle_prefill_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_25_gb300 import build
+    build.build()
+    assert pa.pa_get_device_error() == 0
+
+
+def _run_case(seed, specs, n_q, n_kv, d, bs, dtype, out_dtype=torch.float32):
+    """specs: list of (cached tokens, chunk).  Writes the context and the chunk
+    through pa_reshape_and_cache, runs pa_prefill_chunk, returns (out, ref)."""
+    rng = np.random.default_rng(seed)
+    R = len(specs)
+    lens = [c + n for c, n in specs]
+    nb = sum(-(-L // bs) for L in lens) + 5
+    order = rng.permutation(nb).astype(np.int32)
+    alloc = pa.Allocator(nb, order)
+    mb = max(-(-L // bs) for L in lens)
+    tables = alloc.build_tables(lens, mb, bs)
+    g = torch.Generator().manual_seed(seed)
+    ks = [torch.randn(L, n_kv, d, generator=g).to(dtype) for L in lens]
+    vs = [torch.randn(L, n_kv, d, generator=g).to(dtype) for L in lens]
+    qs = [torch.randn(n, n_q, d, generator=g).to(dtype) for _, n in specs]
+    kc = torch.full((nb, n_kv, bs, d), float("nan"), dtype=dtype, device="cuda")
+    vc = kc.clone()
+    seq = np.concatenate([np.full(L, r, np.int32) for r, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
+    slots = torch.from_numpy(pa.pa_slot_mapping(tables, bs, seq, pos)).cuda()
+    pa.pa_reshape_and_cache(torch.cat(ks).cuda(), torch.cat(vs).cuda(), kc, vc, slots)
+    qsl = np.zeros(R + 1, np.int32)
+    qsl[1:] = np.cumsum([n for _, n in specs])
+    out = torch.full((int(qsl[-1]), n_q, d), float("nan"), dtype=out_dtype, device="cuda")
+    pa.pa_prefill_chunk(out, torch.cat(qs).cuda(), kc, vc, torch.from_numpy(tables).cuda(),
+                        torch.from_numpy(qsl).cuda(),
+                        torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                        max(n for _, n in specs), 1.0 / np.sqrt(d), bs)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    ref = np.concatenate(oracle.prefill(qs, ks, vs, scale))
+    return out, ref
+
+
+CASES = [
+    # seed, specs (ctx, chunk), n_q, n_kv, d, bs, dtype
+    (1, [(0, 37)], 4, 4, 64, 16, torch.bfloat16),                         # plain causal prefill
+    (2, [(0, 200), (100, 1), (33, 47)], 32, 8, 128, 16, torch.bfloat16),  # ragged, several tiles
+    (3, [(500, 64), (0, 16), (16, 16)], 8, 1, 64, 32, torch.float16),     # MQA g=8
+    (4, [(1000, 130)], 40, 40, 128, 16, torch.float16),                   # MHA
+    (5, [(47, 200), (1, 3)], 12, 4, 128, 32, torch.bfloat16),             # g=3, rows straddle
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"p{c[0]}" for c in CASES])
+def test_prefill_small_all_rows(case):
+    seed, specs, n_q, n_kv, d, bs, dtype = case
+    out, ref = _run_case(seed, specs, n_q, n_kv, d, bs, dtype)
+    err = max_err(out, ref)
+    assert err <= TOL[dtype], err
+
+
+def test_prefill_bf16_output():
+    out, ref = _run_case(9, [(300, 100), (0, 50)], 32, 8, 128, 16, torch.bfloat16,
+                         out_dtype=torch.bfloat16)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2e-3 + half_ulp(ref, torch.bfloat16))
+
+
+def test_prefill_chunk_of_one_matches_decode():
+    d, bs, n_q, n_kv = 128, 16, 32, 8
+    out, ref = _run_case(11, [(77, 1)], n_q, n_kv, d, bs, torch.bfloat16)
+    assert max_err(out, ref) <= 2e-3
+
+
+def test_prefill_mixed_workload_sampled_rows():
+    wl = inputs.get("mixed-llama3-8b-bf16")
+    st = PagedStep(wl, out_dtype=torch.float32, prefill_out_dtype=torch.float32)
+    st.step()
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    qsl = st.query_start_loc.cpu().numpy()
+    for r in range(st.R):
+        C = int(st.p_chunk[r])
+        rows = sorted({0, 1, 2, C // 2, C - 2, C - 1})
+        ref = oracle_prefill_rows(st, r, rows)
+        got = st.p_out[int(qsl[r]) + np.array(rows)]
+        assert max_err(got, ref) <= 2e-3
+    assert torch.isfinite(st.p_out).all()
