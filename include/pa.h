@@ -120,6 +120,30 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
                                 int block_size, int max_context_len);
 
+/* ---------------------------------------------------------------- decode, no allocation
+ * The paper has no counterpart to this call.  It is pa_decode for callers that
+ * cannot allocate device memory: a host runtime that gives all free HBM to its
+ * KV block pool at start-up and offers plugins no allocator, or a
+ * latency-critical loop that cannot pay for cudaMalloc's device-wide
+ * synchronisation.  Inputs and outputs are exactly those of pa_decode; the
+ * split-K scratch is a fixed array of PA_DECODE_NO_ALLOC_SCRATCH_BYTES inside
+ * the library, present on every GPU that loads it until the process exits.
+ *   - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
+ *   - A batch whose pa_decode_workspace_size(...) exceeds the fixed size is
+ *     rejected with PA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up per device); make that first call before any stream
+ *     capture.
+ *   - All calls share the array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it: serialise them. */
+#define PA_DECODE_NO_ALLOC_SCRATCH_BYTES (16u << 20)
+pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
+                             const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int num_seqs, int n_q_heads,
+                             float scale, int block_size, void* stream);
+
 /* ---------------------------------------------------------------- chunked prefill
  * A chunk of C_r new query rows of request r attends causally over the paged
  * context ("The hands-on guide ...", chunked prefill): query row i sits at

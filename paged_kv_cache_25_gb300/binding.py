@@ -18,6 +18,7 @@ from . import build as _build
 
 __all__ = [
     "PAError", "lib", "pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_size",
+    "pa_decode_no_alloc", "PA_DECODE_NO_ALLOC_SCRATCH_BYTES",
     "pa_prefill_chunk", "pa_prefill_workspace_size", "pa_get_device_error", "pa_status_string",
     "pa_set_profile_events", "Allocator", "pa_slot_mapping", "pa_kv_bytes_per_token",
     "pa_pool_blocks", "EXPORTED", "dtype_code",
@@ -38,6 +39,7 @@ _SIGS = {
     "pa_reshape_and_cache": (I, [P, P, P, P, P, I, C.POINTER(_Desc), P]),
     "pa_decode": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, F, I, P, SZ, P]),
     "pa_decode_workspace_size": (SZ, [I, I, I, I, I, I]),
+    "pa_decode_no_alloc": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, F, I, P]),
     "pa_prefill_chunk": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, P, I, I, I, F, I, P, SZ, P]),
     "pa_prefill_workspace_size": (SZ, [I, I, I, I]),
     "pa_get_device_error": (I, [P]),
@@ -151,6 +153,23 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float
                            int(block_tables.shape[1]), _ptr(context_lens), int(B), int(n_q),
                            float(scale), int(block_size), _ptr(workspace), ws_bytes,
                            _stream(stream)), "pa_decode")
+
+
+def pa_decode_no_alloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                       block_size: int, stream=None):
+    """pa_decode with the library's fixed internal scratch: the caller passes
+    only inputs and outputs and nothing is allocated.  Batches that need more
+    than PA_DECODE_NO_ALLOC_SCRATCH_BYTES of scratch raise PAError."""
+    B, n_q, _ = q.shape
+    d = _desc(k_cache)
+    _check(lib().pa_decode_no_alloc(_ptr(out), dtype_code(out.dtype), _ptr(q), _ptr(k_cache),
+                                    _ptr(v_cache), C.byref(d), _ptr(block_tables),
+                                    int(block_tables.shape[1]), _ptr(context_lens), int(B),
+                                    int(n_q), float(scale), int(block_size), _stream(stream)),
+           "pa_decode_no_alloc")
+
+
+PA_DECODE_NO_ALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def pa_prefill_workspace_size(num_reqs, n_q_heads, head_dim, total_q) -> int:
