@@ -17,6 +17,7 @@ plus decode tokens/s and steps/s.  Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -38,7 +39,11 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic of the main decode kernel on this workload, per launch
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
 # source is byte-identical to what was profiled (sha256 of csrc/decode.cu).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --set full on a 64-sequence case of the same shapes, scaled by unique
+    # K/V bytes to the 256-sequence workload (see profiles/decode_mma_llama3-8b-bf16_b64_full.md)
+    ("llama3-8b-bf16", 256, "665d4727fef49309"): 2400196821,
+}
 
 
 def _peaks():
@@ -203,6 +208,8 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     pa.lib()
     wl = inputs.get(args.workload)
+    if args.batch:
+        wl = dataclasses.replace(wl, batch=args.batch)
     st = PagedStep(wl, seed=wl.seed + rank, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
@@ -301,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
     # bytes plus q, the output/partials are < 0.5% and not counted
     achieved = kv_unique / (dec_ms * 1e-3) / 1e9
     src = _src_hash("decode.cu")
-    tr = NCU_TRAFFIC.get((wl.name, src))
+    tr = NCU_TRAFFIC.get((wl.name, B, src))
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
@@ -346,6 +353,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's decode batch (profiling a smaller case)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
