@@ -56,6 +56,18 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _peaks_tensor():
+    """Dense bf16 tensor peak: the sustained cuBLAS figure (kernels timed inside a
+    long step loop)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops_sustained"]), "bf16_tflops_sustained (measured)"
+    except Exception:
+        return 1700.0, "bf16 sustained (fallback)"
+
+
 def _src_hash(name: str) -> str:
     with open(os.path.join(ROOT, "paged_kv_cache_25_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -223,6 +235,8 @@ def run_ours(args, rank, world, local_rank):
     # ---- device-timed region: inputs resident in HBM ---------------------
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)] if st.R else [None] * args.steps
     for a, b in ev:            # torch creates the CUDA event at its first record
         a.record(stream)
         b.record(stream)
@@ -238,7 +252,7 @@ def run_ours(args, rank, world, local_rank):
     t_start.record(stream)
     for i in range(args.steps):
         pa.pa_set_profile_events(*ev[i])
-        st.step()
+        st.step(prefill_events=pev[i])
     t_stop.record(stream)
     torch.cuda.synchronize(dev)
     pa.pa_set_profile_events(None, None)
@@ -248,6 +262,7 @@ def run_ours(args, rank, world, local_rank):
     assert pa.pa_get_device_error() == 0
     ms_total = t_start.elapsed_time(t_stop)
     decode_ms = [a.elapsed_time(b) for a, b in ev]
+    prefill_ms = [a.elapsed_time(b) for a, b in pev] if st.R else None
 
     # ---- end to end through the public API with host buffers --------------
     B = wl.batch
@@ -334,7 +349,16 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     if st.R:
-        line["prefill_flops_per_step"] = st.prefill_flops()
+        pf_ms = statistics.mean(prefill_ms)
+        flops = st.prefill_flops()
+        tf = _peaks_tensor()
+        line["prefill_flops_per_step"] = flops
+        line["prefill_kernel_ms"] = pf_ms
+        line["roofline_prefill"] = {
+            "bound": "tensor", "achieved": flops / (pf_ms * 1e-3) / 1e12, "peak": tf[0],
+            "unit": "TFLOP/s", "frac": flops / (pf_ms * 1e-3) / 1e12 / tf[0], "traffic": None,
+            "kernel": "prefill_mma_kernel", "peak_source": tf[1]}
+        line["prefill_tokens_per_s"] = world * int(st.p_chunk.sum()) / (ms_step * 1e-3)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, t, desc, threads, _ = oracle_sample(wl.name, None, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",

@@ -104,9 +104,12 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
  *                  undefined output for that sequence).
  *   block_size   : must equal cache->block_size.
  *   workspace    : device scratch of at least pa_decode_workspace_size(...)
- *                  bytes for the same shapes, 256-byte aligned; NULL allowed
- *                  when that size is 0.  Long contexts are split over several
- *                  thread blocks and combined by a second kernel through it.
+ *                  bytes for the same shapes, 256-byte aligned; its contents
+ *                  need no initialisation.  It holds the work counter of the
+ *                  persistent decode kernel (reset on the stream by each call)
+ *                  and, for long contexts split over several thread blocks,
+ *                  the partial results the second kernel combines.  Calls that
+ *                  overlap on the GPU must not share one workspace.
  * n_q_heads must be a multiple of n_kv_heads.  Accumulation is fp32. */
 pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
                     const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
@@ -116,7 +119,8 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace pa_decode needs for sequences of at most max_context_len
- * tokens (0 when no sequence is long enough to be split). */
+ * tokens (pass max_blocks_per_seq * block_size of the tables you will pass);
+ * at least 256. */
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
                                 int block_size, int max_context_len);
 
@@ -134,9 +138,10 @@ size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int n_kv_heads, int
  *   - The first call on a device looks up the array's device address (a
  *     one-time set-up per device); make that first call before any stream
  *     capture.
- *   - All calls share the array and it keeps the last call's contents;
- *     nothing in it needs to start at zero.  Calls that overlap on the GPU
- *     (other streams, other host threads) race on it: serialise them. */
+ *   - All calls share the array and it keeps the last call's contents; what
+ *     must start at zero (the work counter) is cleared on the stream by every
+ *     call.  Calls that overlap on the GPU (other streams, other host threads)
+ *     race on it: serialise them. */
 #define PA_DECODE_NO_ALLOC_SCRATCH_BYTES (16u << 20)
 pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
                              const void* k_cache, const void* v_cache, const pa_cache_desc* cache,

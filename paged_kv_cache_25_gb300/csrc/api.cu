@@ -104,10 +104,11 @@ int decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int ma
 {
     // 512 tokens (32 or 16 blocks) per partition keeps the split-K overhead at
     // a few percent of the K/V bytes; halve it (down to 128) while the batch
-    // would offer fewer than ~1024 units of work to the GPU.
+    // would offer fewer than ~8 units of work per resident CTA (2 per SM on
+    // 152 SMs).
     int p = 512;
     while (p > 128 && p > block_size &&
-           static_cast<int64_t>(num_seqs) * n_kv_heads * ((max_context_len + p - 1) / p) < 1024)
+           static_cast<int64_t>(num_seqs) * n_kv_heads * ((max_context_len + p - 1) / p) < 2432)
         p /= 2;
     return p;
 }
@@ -133,6 +134,11 @@ static pa_status check_cache(const pa_cache_desc* c)
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace: a 256-byte control area (the decode's work counter), then, when
+// some sequence can span several partitions, (m, l) [B][n_q][J][2] and the
+// partial outputs [B][n_q][J][D], all fp32.
+static constexpr size_t kControlBytes = 256;
+
 static size_t decode_ws_bytes(int B, int n_q, int n_kv, int D, int BS, int max_ctx, int* part,
                               int* parts)
 {
@@ -140,9 +146,9 @@ static size_t decode_ws_bytes(int B, int n_q, int n_kv, int D, int BS, int max_c
     const int J = (max_ctx + p - 1) / p;
     if (part) *part = p;
     if (parts) *parts = J < 1 ? 1 : J;
-    if (J <= 1) return 0;
+    if (J <= 1) return kControlBytes;
     const size_t units = static_cast<size_t>(B) * n_q * J;
-    return align256(units * 2 * sizeof(float)) + units * D * sizeof(float);
+    return kControlBytes + align256(units * 2 * sizeof(float)) + units * D * sizeof(float);
 }
 
 }  // namespace pa
@@ -256,13 +262,11 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_
     const size_t need = decode_ws_bytes(num_seqs, n_q_heads, cache->n_kv_heads, cache->head_dim,
                                         block_size, max_ctx, &part, &parts);
     if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions per sequence");
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need)
-            return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
-                        workspace ? workspace_bytes : (size_t)0);
-        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-            return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    }
+    if (!workspace || workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     unsigned* err = device_error_word();
     if (!err) return fail(PA_ERR_CUDA, "cannot locate the device error word");
 
@@ -272,11 +276,12 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_
     a.block_tables = block_tables; a.max_blocks = max_blocks_per_seq;
     a.context_lens = context_lens; a.num_seqs = num_seqs; a.n_q = n_q_heads; a.scale = scale;
     a.part_tokens = part; a.max_parts = parts; a.err = err;
-    if (need > 0) {
+    a.ticket = static_cast<unsigned*>(workspace);
+    if (need > kControlBytes) {
         const size_t units = static_cast<size_t>(num_seqs) * n_q_heads * parts;
-        a.ws_ml = static_cast<float*>(workspace);
-        a.ws_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                            align256(units * 2 * sizeof(float)));
+        char* base = static_cast<char*>(workspace) + kControlBytes;
+        a.ws_ml = reinterpret_cast<float*>(base);
+        a.ws_acc = reinterpret_cast<float*>(base + align256(units * 2 * sizeof(float)));
     }
     cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");

@@ -3,17 +3,22 @@
 // actually reads paged blocks": look the block up once, q.k against its keys,
 // softmax-weighted sum of its values).
 //
-// Work unit = (sequence s, KV head, partition j of part_tokens tokens).  Long
-// contexts are split into partitions whose (max, sum, unnormalised output)
-// are combined by decode_reduce_kernel; a sequence that fits in one
-// partition is finished by the partition kernel itself.
+// Work unit = (sequence s, KV head [8-head sub-group], partition j of
+// part_tokens tokens).  Long contexts are split into partitions whose (max,
+// sum, unnormalised output) are combined by decode_reduce_kernel; a sequence
+// that fits in one partition is finished by the partition kernel itself.
 //
-// Tensor-core path (bf16/fp16, head_dim 64/128, block 16/32):
+// Tensor-core path (bf16/fp16, head_dim 64/128, block 16/32), persistent:
+//   - a grid of (SMs x resident CTAs) walks a compact list of the live units:
+//     each CTA builds the prefix sum of partitions per sequence in shared
+//     memory and maps unit numbers to (sequence, partition, head group) by
+//     binary search, so skewed lengths cost no empty CTAs;
 //   - the g query heads sharing one KV head form the M rows of an m16n8k16
 //     MMA, so each K/V slab is read from HBM once for the whole group;
-//   - each warp owns a ring of NS stages; lane 0 streams whole
-//     (block, kv head) slabs of K and V into it with 2-D TMA tile loads
-//     (128-byte swizzle, so ldmatrix reads are bank-conflict free);
+//   - each warp owns a ring of NS stages of 16 K/V rows; lane 0 streams them
+//     with 2-D TMA tile loads (128-byte swizzle, so ldmatrix reads are bank
+//     conflict free); a 32-token block is two stages, so the ring and the
+//     occupancy do not depend on the block size;
 //   - online softmax in registers with quad shuffles;
 //   - P is split into hi + lo halves of the input type and placed in rows
 //     0-7 and 8-15 of the A operand, so P.V costs one MMA yet keeps ~16 bits
@@ -26,10 +31,14 @@
 
 #include <math.h>
 
+#include <mutex>
+
 namespace pa {
 
 constexpr int kDecWarps = 4;
-constexpr int kMaxPartBlocks = 64;
+constexpr int kRows = 16;            // K/V rows per pipeline stage
+constexpr int kMaxPartBlocks = 64;   // blocks per partition (part_tokens / block_size)
+constexpr int kPrefixCap = 2048;     // sequences whose partition prefix sum fits in smem
 
 __device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dtype dt)
 {
@@ -41,258 +50,342 @@ __device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dt
         static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
-template <typename T, int D, int BS, int NS>
+template <typename T, int D, int NS>
 struct DecodeCfg {
-    static constexpr int kSlabBytes = BS * D * static_cast<int>(sizeof(T));  // one K (or V) slab
+    static constexpr int kSlabBytes = kRows * D * static_cast<int>(sizeof(T));  // 16 rows of K or V
     static constexpr int kStageBytes = 2 * kSlabBytes;
     static constexpr int kWarpBytes = NS * kStageBytes;
     static constexpr int kRingBytes = kDecWarps * kWarpBytes;
     static constexpr int kReduceBytes = kDecWarps * 8 * (D + 2) * 4;
     static constexpr int kDynBytes = (kRingBytes > kReduceBytes ? kRingBytes : kReduceBytes) + 1024;
     static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
-    static_assert(BS % 16 == 0, "block_size must be a multiple of 16");
 };
 
 template <typename T, int D, int BS, int NS>
-__global__ void __launch_bounds__(kDecWarps * 32)
+__global__ void __launch_bounds__(kDecWarps * 32, 2)
 decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   void* __restrict__ out, pa_dtype out_dtype, const T* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
-                  const int32_t* __restrict__ context_lens, int n_q, int n_kv, int group,
-                  int num_blocks, float scale_log2, float* __restrict__ ws_ml,
-                  float* __restrict__ ws_acc, int part_tokens, int max_parts, unsigned* err)
+                  const int32_t* __restrict__ context_lens, int num_seqs, int n_q, int n_kv,
+                  int group, int num_blocks, float scale_log2, float* __restrict__ ws_ml,
+                  float* __restrict__ ws_acc, int part_tokens, int max_parts,
+                  unsigned* __restrict__ ticket, unsigned* err)
 {
-    using Cfg = DecodeCfg<T, D, BS, NS>;
-    constexpr int kHalf = 64;              // elements per 128-byte swizzled row
-    constexpr int kHalves = D / kHalf;
-    constexpr int kHalfTileBytes = BS * 128;
+    using Cfg = DecodeCfg<T, D, NS>;
+    constexpr int kHalves = D / 64;           // 64-column halves (one 128-byte swizzled row each)
+    constexpr int kHalfTile = kRows * 128;
+    constexpr int kCPB = BS / kRows;          // stages per block
+    static_assert(BS % kRows == 0, "block_size must be a multiple of 16");
 
-    const int j = blockIdx.x;
-    const int n_sub = (group + 7) >> 3;
-    const int kvh = blockIdx.y / n_sub;
-    const int sub = blockIdx.y - kvh * n_sub;
-    const int s = blockIdx.z;
-    const int h0 = kvh * group + sub * 8;
-    const int nh = min(8, group - sub * 8);
-
-    const int L = __ldg(context_lens + s);
-    const int tok0 = j * part_tokens;
-    if (tok0 >= L) return;
-    const int tok1 = min(L, tok0 + part_tokens);
-    const int nblk = (tok1 - tok0 + BS - 1) / BS;
-    const int blk0 = tok0 / BS;
-    const int nparts = min((L + part_tokens - 1) / part_tokens, max_parts);
-
+    __shared__ int s_prefix[kPrefixCap];
+    __shared__ int s_scan[kDecWarps * 32];
     __shared__ int s_blk[kMaxPartBlocks];
-    __shared__ int s_bad;
+    __shared__ int s_total;
+    __shared__ long long s_next;
     __shared__ __align__(8) uint64_t s_bar[kDecWarps * NS];
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) s_bad = 0;
-    __syncthreads();
-    for (int i = tid; i < nblk; i += blockDim.x) {
-        const int lb = blk0 + i;
-        int b = -1;
-        if (lb < max_blocks) b = __ldg(block_tables + static_cast<int64_t>(s) * max_blocks + lb);
-        if (b < 0 || b >= num_blocks) {
-            s_bad = 1;
-            set_error(err, PA_ERR_OUT_OF_RANGE);
+    const int n_sub = (group + 7) >> 3;
+    const int n_groups = n_kv * n_sub;
+    const bool use_prefix = num_seqs <= kPrefixCap;
+
+    // ---- units: first every full partition, then every sequence's last one.
+    // The last partitions are the ragged, cheaper units, so handing them out
+    // last evens out the tail of the static round-robin assignment.
+    // s_prefix[s] = inclusive prefix sum of (partitions of s) - 1.
+    if (use_prefix) {
+        const int per = (num_seqs + kDecWarps * 32 - 1) / (kDecWarps * 32);
+        const int b0 = tid * per, b1 = min(num_seqs, b0 + per);
+        int local = 0;
+        for (int i = b0; i < b1; ++i) {
+            const int L = __ldg(context_lens + i);
+            const int p = L > 0 ? min((L + part_tokens - 1) / part_tokens, max_parts) - 1 : 0;
+            s_prefix[i] = p;
+            local += p;
         }
-        s_blk[i] = b;
+        s_scan[tid] = local;
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            for (int i = 0; i < kDecWarps * 32; ++i) {
+                const int v = s_scan[i];
+                s_scan[i] = acc;
+                acc += v;
+            }
+            s_total = acc;                  // full partitions
+        }
+        __syncthreads();
+        int run = s_scan[tid];
+        for (int i = b0; i < b1; ++i) {
+            run += s_prefix[i];
+            s_prefix[i] = run;
+        }
+    } else if (tid == 0) {
+        s_total = num_seqs * (max_parts - 1);
     }
     if (tid < kDecWarps * NS) mbar_init(smem_u32(&s_bar[tid]), 1);
     fence_mbar_init();
     __syncthreads();
-    if (s_bad) return;
 
-    // ---- per-warp TMA ring --------------------------------------------
+    const int n_full = s_total;
+    const int64_t units = (static_cast<int64_t>(n_full) + num_seqs) * n_groups;
     const uint32_t ring = smem_u32(smem) + warp * Cfg::kWarpBytes;
     const uint32_t bar0 = smem_u32(&s_bar[warp * NS]);
-    const int my_n = nblk > warp ? (nblk - warp + kDecWarps - 1) / kDecWarps : 0;
-
-    auto issue = [&](int k) {
-        const int b = s_blk[warp + k * kDecWarps];
-        const int st = k % NS;
-        const uint32_t kdst = ring + st * Cfg::kStageBytes;
-        const uint32_t vdst = kdst + Cfg::kSlabBytes;
-        const uint32_t bar = bar0 + st * 8;
-        const int row = (b * n_kv + kvh) * BS;
-        mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
-#pragma unroll
-        for (int hx = 0; hx < kHalves; ++hx) {
-            tma_load_2d(kdst + hx * kHalfTileBytes, &kmap, hx * kHalf, row, bar);
-            tma_load_2d(vdst + hx * kHalfTileBytes, &vmap, hx * kHalf, row, bar);
-        }
-    };
+    const int g = lane >> 2, t4 = lane & 3;
+    uint32_t kt = 0;   // stages this warp has consumed so far: its ring position and phase
     if (lane == 0) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
-        for (int k = 0; k < min(NS, my_n); ++k) issue(k);
     }
 
-    // ---- query fragments: rows 0-7 = heads of the sub-group, rows 8-15 zero
-    const int g = lane >> 2, t4 = lane & 3;
-    uint32_t qa[D / 16][2];
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        if (g < nh) {
-            const T* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
-            qa[kk][0] = __ldg(reinterpret_cast<const unsigned int*>(qp));
-            qa[kk][1] = __ldg(reinterpret_cast<const unsigned int*>(qp + 8));
+    // Units are handed out dynamically: unit blockIdx.x first, then tickets
+    // from a counter that starts at zero for every launch.  The ticket for the
+    // next unit is fetched while the current one streams.
+    int64_t u = blockIdx.x;
+    while (u < units) {
+        const int gp = static_cast<int>(u / n_groups);
+        const int grp = static_cast<int>(u - static_cast<int64_t>(gp) * n_groups);
+        int s, part;
+        if (gp >= n_full) {                           // a sequence's last partition
+            s = gp - n_full;
+            const int Ls = __ldg(context_lens + s);
+            part = Ls > 0 ? min((Ls + part_tokens - 1) / part_tokens, max_parts) - 1 : 0;
+        } else if (use_prefix) {
+            int lo = 0, hi = num_seqs - 1;            // first s with prefix[s] > gp
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (s_prefix[mid] > gp) hi = mid; else lo = mid + 1;
+            }
+            s = lo;
+            part = gp - (s ? s_prefix[s - 1] : 0);
         } else {
-            qa[kk][0] = 0u;
-            qa[kk][1] = 0u;
+            s = gp / (max_parts - 1);
+            part = gp - s * (max_parts - 1);
         }
-    }
+        const int L = __ldg(context_lens + s);
+        const int tok0 = part * part_tokens;
+        const bool live = tok0 < L;                   // same decision in every thread
+        const int kvh = grp / n_sub, sub = grp - (grp / n_sub) * n_sub;
+        const int h0 = kvh * group + sub * 8;
+        const int nh = min(8, group - sub * 8);
+        const int tok1 = min(L, tok0 + part_tokens);
+        const int nblk = (tok1 - tok0 + BS - 1) / BS;
+        const int nchunk = (tok1 - tok0 + kRows - 1) / kRows;
+        const int blk0 = tok0 / BS;
+        const int nparts = min((L + part_tokens - 1) / part_tokens, max_parts);
 
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-
-    for (int k = 0; k < my_n; ++k) {
-        const int st = k % NS;
-        const bool ok = mbar_wait(bar0 + st * 8, (k / NS) & 1, err);
-        if (!__all_sync(0xffffffffu, ok)) break;   // leave together: shuffles follow
-        const int pos0 = tok0 + (warp + k * kDecWarps) * BS;
-        const int valid = min(BS, L - pos0);
-        const uint32_t kbase = ring + st * Cfg::kStageBytes;
-        const uint32_t vbase = kbase + Cfg::kSlabBytes;
-
-        if (valid < BS) {
-            // rows past the sequence may hold anything (even NaN): zero them in
-            // V so that 0 * row stays 0 inside the MMA
-            uint8_t* vgen = smem + (vbase - smem_u32(smem));
-            const int nbytes = (BS - valid) * 128;
-            for (int hx = 0; hx < kHalves; ++hx)
-                for (int off = lane * 16; off < nbytes; off += 32 * 16)
-                    *reinterpret_cast<uint4*>(vgen + hx * kHalfTileBytes + valid * 128 + off) =
-                        make_uint4(0, 0, 0, 0);
-            __syncwarp();
+        // block ids of the partition, range-checked before any load is issued
+        int bad = 0;
+        for (int i = tid; live && i < nblk; i += kDecWarps * 32) {
+            const int lb = blk0 + i;
+            int b = -1;
+            if (lb < max_blocks) b = __ldg(block_tables + static_cast<int64_t>(s) * max_blocks + lb);
+            if (b < 0 || b >= num_blocks) {
+                bad = 1;
+                set_error(err, PA_ERR_OUT_OF_RANGE);
+            }
+            s_blk[i] = b;
+        }
+        const int any_bad = __syncthreads_or(bad);   // also: everyone has read s_next
+        if (tid == 0) s_next = static_cast<long long>(gridDim.x) + atomicAdd(ticket, 1u);
+        if (!live || any_bad) {
+            __syncthreads();
+            u = s_next;
+            continue;
         }
 
-        // S = Q K^T for the BS tokens of the block
-        float sc[BS / 8][4];
+        // ---- per-warp TMA ring over the partition's 16-row stages --------
+        const int my_n = nchunk > warp ? (nchunk - warp + kDecWarps - 1) / kDecWarps : 0;
+        auto issue = [&](int k) {
+            const int c = warp + k * kDecWarps;
+            const int b = s_blk[c / kCPB];
+            const uint32_t st = (kt + k) % NS;
+            const uint32_t kdst = ring + st * Cfg::kStageBytes;
+            const uint32_t vdst = kdst + Cfg::kSlabBytes;
+            const uint32_t bar = bar0 + st * 8;
+            const int row = (b * n_kv + kvh) * BS + (c % kCPB) * kRows;
+            mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
 #pragma unroll
-        for (int nt = 0; nt < BS / 8; ++nt) {
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            for (int hx = 0; hx < kHalves; ++hx) {
+                tma_load_2d(kdst + hx * kHalfTile, &kmap, hx * 64, row, bar);
+                tma_load_2d(vdst + hx * kHalfTile, &vmap, hx * 64, row, bar);
+            }
+        };
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            for (int k = 0; k < min(NS, my_n); ++k) issue(k);
+        }
+
+        // query fragments: rows 0-7 = heads of the sub-group, rows 8-15 zero
+        uint32_t qa[D / 16][2];
 #pragma unroll
-            for (int kc = 0; kc < D / 16; kc += 2) {
-                const int r = nt * 8 + (lane & 7);
-                const int chunk = kc * 2 + (lane >> 3);
-                const uint32_t addr = kbase + (chunk >> 3) * kHalfTileBytes + r * 128 +
-                                      (((chunk & 7) ^ (r & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(addr, b0, b1, b2, b3);
-                const uint32_t a0[4] = {qa[kc][0], 0u, qa[kc][1], 0u};
-                const uint32_t a1[4] = {qa[kc + 1][0], 0u, qa[kc + 1][1], 0u};
-                MmaOp<T>::run(sc[nt], a0, b0, b1);
-                MmaOp<T>::run(sc[nt], a1, b2, b3);
+        for (int kk = 0; kk < D / 16; ++kk) {
+            if (g < nh) {
+                const T* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
+                qa[kk][0] = __ldg(reinterpret_cast<const unsigned int*>(qp));
+                qa[kk][1] = __ldg(reinterpret_cast<const unsigned int*>(qp + 8));
+            } else {
+                qa[kk][0] = 0u;
+                qa[kk][1] = 0u;
             }
         }
 
-        // online softmax on row g (log2 domain)
-        float mx = -INFINITY;
+        float o[D / 8][4];
 #pragma unroll
-        for (int nt = 0; nt < BS / 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int p = pos0 + nt * 8 + 2 * t4 + e;
-                const float z = p < L ? sc[nt][e] * scale_log2 : -INFINITY;
-                sc[nt][e] = z;
-                mx = fmaxf(mx, z);
-            }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2f(m_run - m_new);
-        m_run = m_new;
-        float psum = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < BS / 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float p = exp2f(sc[nt][e] - m_new);
-                sc[nt][e] = p;
-                psum += p;
-            }
-        l_run = l_run * alpha + psum;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha; o[i][3] *= alpha;
-        }
+        for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;
+        int timed_out = 0;
 
-        // O += P V, P as hi (rows 0-7) + lo (rows 8-15)
+        for (int k = 0; k < my_n; ++k) {
+            const uint32_t st = (kt + k) % NS;
+            const bool ok = mbar_wait(bar0 + st * 8, ((kt + k) / NS) & 1u, err);
+            if (!__all_sync(0xffffffffu, ok)) {     // leave together: shuffles follow
+                timed_out = 1;
+                break;
+            }
+            const int pos0 = tok0 + (warp + k * kDecWarps) * kRows;
+            const int valid = min(kRows, L - pos0);
+            const uint32_t kbase = ring + st * Cfg::kStageBytes;
+            const uint32_t vbase = kbase + Cfg::kSlabBytes;
+
+            if (valid < kRows) {
+                // rows past the sequence may hold anything (even NaN): zero them in
+                // V so that 0 * row stays 0 inside the MMA
+                uint8_t* vgen = smem + (vbase - smem_u32(smem));
+                const int nbytes = (kRows - valid) * 128;
+                for (int hx = 0; hx < kHalves; ++hx)
+                    for (int off = lane * 16; off < nbytes; off += 32 * 16)
+                        *reinterpret_cast<uint4*>(vgen + hx * kHalfTile + valid * 128 + off) =
+                            make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+
+            // S = Q K^T for the 16 rows
+            float sc[2][4];
 #pragma unroll
-        for (int ks = 0; ks < BS / 16; ++ks) {
+            for (int nt = 0; nt < 2; ++nt) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+                for (int kc = 0; kc < D / 16; kc += 2) {
+                    const int r = nt * 8 + (lane & 7);
+                    const int chunk = kc * 2 + (lane >> 3);
+                    const uint32_t addr = kbase + (chunk >> 3) * kHalfTile + r * 128 +
+                                          (((chunk & 7) ^ (r & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(addr, b0, b1, b2, b3);
+                    const uint32_t a0[4] = {qa[kc][0], 0u, qa[kc][1], 0u};
+                    const uint32_t a1[4] = {qa[kc + 1][0], 0u, qa[kc + 1][1], 0u};
+                    MmaOp<T>::run(sc[nt], a0, b0, b1);
+                    MmaOp<T>::run(sc[nt], a1, b2, b3);
+                }
+            }
+
+            // online softmax on row g (log2 domain)
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int p = pos0 + nt * 8 + 2 * t4 + e;
+                    const float z = p < L ? sc[nt][e] * scale_log2 : -INFINITY;
+                    sc[nt][e] = z;
+                    mx = fmaxf(mx, z);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = exp2f(m_run - m_new);
+            m_run = m_new;
+            float psum = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float p = exp2f(sc[nt][e] - m_new);
+                    sc[nt][e] = p;
+                    psum += p;
+                }
+            l_run = l_run * alpha + psum;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha; o[i][3] *= alpha;
+            }
+
+            // O += P V, P as hi (rows 0-7) + lo (rows 8-15)
             uint32_t pa[4];
-            split_pair<T>(sc[2 * ks][0], sc[2 * ks][1], pa[0], pa[1]);
-            split_pair<T>(sc[2 * ks + 1][0], sc[2 * ks + 1][1], pa[2], pa[3]);
+            split_pair<T>(sc[0][0], sc[0][1], pa[0], pa[1]);
+            split_pair<T>(sc[1][0], sc[1][1], pa[2], pa[3]);
 #pragma unroll
             for (int nt = 0; nt < D / 8; nt += 2) {
                 const int mi = lane >> 3;
-                const int r = ks * 16 + (mi & 1) * 8 + (lane & 7);
+                const int r = (mi & 1) * 8 + (lane & 7);
                 const int chunk = nt + (mi >> 1);
-                const uint32_t addr = vbase + (chunk >> 3) * kHalfTileBytes + r * 128 +
+                const uint32_t addr = vbase + (chunk >> 3) * kHalfTile + r * 128 +
                                       (((chunk & 7) ^ (r & 7)) << 4);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_t(addr, b0, b1, b2, b3);
                 MmaOp<T>::run(o[nt], pa, b0, b1);
                 MmaOp<T>::run(o[nt + 1], pa, b2, b3);
             }
-        }
 
-        __syncwarp();
-        if (lane == 0 && k + NS < my_n) {
-            fence_proxy_async_smem();
-            issue(k + NS);
-        }
-    }
-
-    // ---- combine the warps ------------------------------------------------
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    __syncthreads();  // every warp is done with its ring: reuse it
-    float* red_o = reinterpret_cast<float*>(smem);              // [warps][8][D]
-    float* red_m = red_o + kDecWarps * 8 * D;                   // [warps][8]
-    float* red_l = red_m + kDecWarps * 8;                       // [warps][8]
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-        float* dst = red_o + (warp * 8 + g) * D + nt * 8 + 2 * t4;
-        dst[0] = o[nt][0] + o[nt][2];
-        dst[1] = o[nt][1] + o[nt][3];
-    }
-    if (t4 == 0) {
-        red_m[warp * 8 + g] = m_run;
-        red_l[warp * 8 + g] = l_run;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nh * D; idx += blockDim.x) {
-        const int hh = idx / D, dd = idx - hh * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
-        float lsum = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) {
-            const float f = exp2f(red_m[w * 8 + hh] - M);
-            lsum += f * red_l[w * 8 + hh];
-            acc += f * red_o[(w * 8 + hh) * D + dd];
-        }
-        const int64_t sh = static_cast<int64_t>(s) * n_q + h0 + hh;
-        if (nparts == 1) {
-            store_any(out, sh * D + dd, acc / lsum, out_dtype);
-        } else {
-            const int64_t u = sh * max_parts + j;
-            ws_acc[u * D + dd] = acc;
-            if (dd == 0) {
-                ws_ml[2 * u] = M;
-                ws_ml[2 * u + 1] = lsum;
+            __syncwarp();
+            if (lane == 0 && k + NS < my_n) {
+                fence_proxy_async_smem();
+                issue(k + NS);
             }
         }
+        kt += my_n;
+
+        // ---- combine the warps ---------------------------------------------
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+        if (__syncthreads_or(timed_out)) return;   // every ring is idle from here on
+        float* red_o = reinterpret_cast<float*>(smem);              // [warps][8][D]
+        float* red_m = red_o + kDecWarps * 8 * D;                   // [warps][8]
+        float* red_l = red_m + kDecWarps * 8;                       // [warps][8]
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+            float* dst = red_o + (warp * 8 + g) * D + nt * 8 + 2 * t4;
+            dst[0] = o[nt][0] + o[nt][2];
+            dst[1] = o[nt][1] + o[nt][3];
+        }
+        if (t4 == 0) {
+            red_m[warp * 8 + g] = m_run;
+            red_l[warp * 8 + g] = l_run;
+        }
+        fence_proxy_async_smem();   // these generic writes precede later TMA writes here
+        __syncthreads();
+        for (int idx = tid; idx < nh * D; idx += kDecWarps * 32) {
+            const int hh = idx / D, dd = idx - hh * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
+            float lsum = 0.f, acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) {
+                const float f = exp2f(red_m[w * 8 + hh] - M);
+                lsum += f * red_l[w * 8 + hh];
+                acc += f * red_o[(w * 8 + hh) * D + dd];
+            }
+            const int64_t sh = static_cast<int64_t>(s) * n_q + h0 + hh;
+            if (nparts == 1) {
+                store_any(out, sh * D + dd, acc / lsum, out_dtype);
+            } else {
+                const int64_t w_idx = sh * max_parts + part;
+                ws_acc[w_idx * D + dd] = acc;
+                if (dd == 0) {
+                    ws_ml[2 * w_idx] = M;
+                    ws_ml[2 * w_idx + 1] = lsum;
+                }
+            }
+        }
+        // the next unit's first barrier (after its block-id checks) orders these
+        // reads before any TMA write into the ring
+        u = s_next;
     }
 }
 
@@ -370,60 +463,97 @@ decode_simt_kernel(void* __restrict__ out, pa_dtype out_dtype, const T* __restri
     }
 }
 
-// Second pass: out = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j.
+// Second pass, one warp per (sequence, query head):
+//   out = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j.
+template <int DPL>
 __global__ void __launch_bounds__(128)
 decode_reduce_kernel(void* __restrict__ out, pa_dtype out_dtype,
                      const int32_t* __restrict__ context_lens, const float* __restrict__ ws_ml,
-                     const float* __restrict__ ws_acc, int n_q, int head_dim, int part_tokens,
+                     const float* __restrict__ ws_acc, int num_seqs, int n_q, int part_tokens,
                      int max_parts)
 {
-    const int h = blockIdx.x, s = blockIdx.y;
+    constexpr int D = DPL * 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t sh = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    if (sh >= static_cast<int64_t>(num_seqs) * n_q) return;
+    const int s = static_cast<int>(sh / n_q);
     const int L = __ldg(context_lens + s);
     const int J = min((L + part_tokens - 1) / part_tokens, max_parts);
     if (J <= 1) return;
-    const int64_t sh = static_cast<int64_t>(s) * n_q + h;
     const float* ml = ws_ml + 2 * sh * max_parts;
     float M = -INFINITY;
-    for (int jj = 0; jj < J; ++jj) M = fmaxf(M, ml[2 * jj]);
+    for (int jj = lane; jj < J; jj += 32) M = fmaxf(M, ml[2 * jj]);
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, w));
     float lsum = 0.f;
-    for (int jj = 0; jj < J; ++jj) lsum += exp2f(ml[2 * jj] - M) * ml[2 * jj + 1];
-    const float inv = 1.f / lsum;
-    for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
-        float acc = 0.f;
-        for (int jj = 0; jj < J; ++jj)
-            acc += exp2f(ml[2 * jj] - M) * ws_acc[(sh * max_parts + jj) * head_dim + d];
-        store_any(out, sh * head_dim + d, acc * inv, out_dtype);
+    float acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+    const float* a = ws_acc + sh * max_parts * D;
+    for (int jj = 0; jj < J; ++jj) {
+        const float w = exp2f(ml[2 * jj] - M);
+        lsum += w * ml[2 * jj + 1];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(w, a[jj * D + lane + 32 * i], acc[i]);
     }
+    const float inv = 1.f / lsum;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) store_any(out, sh * D + lane + 32 * i, acc[i] * inv, out_dtype);
 }
 
 // ------------------------------------------------------------------ launch
+
+static int sm_count()
+{
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
 
 template <typename T, int D, int BS>
 static cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
 {
     // ring depth per warp: about 24 KB of K+V in flight per warp, at least 2 stages
-    constexpr int kStage = 2 * BS * D * static_cast<int>(sizeof(T));
+    constexpr int kStage = 2 * kRows * D * static_cast<int>(sizeof(T));
     constexpr int NS = 24576 / kStage > 2 ? 24576 / kStage : 2;
-    using Cfg = DecodeCfg<T, D, BS, NS>;
+    using Cfg = DecodeCfg<T, D, NS>;
     auto kern = decode_mma_kernel<T, D, BS, NS>;
-    static bool attr_done = false;   // per process; the attribute is per function
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg::kDynBytes);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int per_sm = 1;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        Cfg::kDynBytes);
+        if (attr_err == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecWarps * 32,
+                                                          Cfg::kDynBytes) != cudaSuccess)
+            per_sm = 1;
+        if (per_sm < 1) per_sm = 1;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap kmap, vmap;
     const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
-    if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, BS) != PA_OK ||
-        encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, BS) != PA_OK)
+    if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK ||
+        encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK)
         return cudaErrorInvalidValue;
     const int group = a.n_q / a.cache.n_kv_heads;
-    dim3 grid(a.max_parts, a.cache.n_kv_heads * ((group + 7) / 8), a.num_seqs);
+    const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.max_parts * a.cache.n_kv_heads *
+                          ((group + 7) / 8);
+    const int64_t resident = static_cast<int64_t>(sm_count()) * per_sm;
+    const unsigned grid = static_cast<unsigned>(upper < resident ? upper : resident);
     kern<<<grid, kDecWarps * 32, Cfg::kDynBytes, s>>>(
         kmap, vmap, a.out, a.out_dtype, static_cast<const T*>(a.q), a.block_tables, a.max_blocks,
-        a.context_lens, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks, scale_log2, a.ws_ml,
-        a.ws_acc, a.part_tokens, a.max_parts, a.err);
+        a.context_lens, a.num_seqs, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
+        scale_log2, a.ws_ml, a.ws_acc, a.part_tokens, a.max_parts, a.ticket, a.err);
     return cudaGetLastError();
 }
 
@@ -463,9 +593,33 @@ static cudaError_t run_mma_dt(const DecodeArgs& a, cudaStream_t s, float sl2)
     return run_simt_dt<T>(a, s, sl2);
 }
 
+static cudaError_t run_reduce(const DecodeArgs& a, cudaStream_t s)
+{
+    const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.n_q;
+    const unsigned grid = static_cast<unsigned>((pairs + 3) / 4);
+#define PA_REDUCE(DPL)                                                                          \
+    decode_reduce_kernel<DPL><<<grid, 128, 0, s>>>(a.out, a.out_dtype, a.context_lens, a.ws_ml, \
+                                                   a.ws_acc, a.num_seqs, a.n_q, a.part_tokens,  \
+                                                   a.max_parts)
+    switch (a.cache.head_dim) {
+        case 32: PA_REDUCE(1); break;
+        case 64: PA_REDUCE(2); break;
+        case 96: PA_REDUCE(3); break;
+        case 128: PA_REDUCE(4); break;
+        case 256: PA_REDUCE(8); break;
+        default: return cudaErrorInvalidValue;
+    }
+#undef PA_REDUCE
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
 {
     const float sl2 = a.scale * 1.4426950408889634f;   // softmax in base 2
+    if (a.cache.dtype != PA_F32) {
+        cudaError_t e0 = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), s);
+        if (e0 != cudaSuccess) return e0;
+    }
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     profile_events(&ev0, &ev1);
     if (ev0) cudaEventRecord(ev0, s);
@@ -477,13 +631,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     }
     if (ev1) cudaEventRecord(ev1, s);
     if (e != cudaSuccess) return e;
-    if (a.max_parts > 1) {
-        dim3 grid(a.n_q, a.num_seqs);
-        decode_reduce_kernel<<<grid, 128, 0, s>>>(a.out, a.out_dtype, a.context_lens, a.ws_ml,
-                                                  a.ws_acc, a.n_q, a.cache.head_dim,
-                                                  a.part_tokens, a.max_parts);
-        e = cudaGetLastError();
-    }
+    if (a.max_parts > 1) e = run_reduce(a, s);
     return e;
 }
 

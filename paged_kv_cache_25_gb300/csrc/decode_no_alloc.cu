@@ -8,10 +8,11 @@
 // device array declared below, so it allocates nothing.
 //
 // The array lives on every GPU that loads the library, until the process
-// exits.  All calls share it and it keeps the previous call's contents;
-// nothing in it needs to start at zero (every partial the reduce reads is
-// written earlier in the same call).  Calls whose work overlaps on the GPU
-// (different streams, or several host threads) race on it.
+// exits.  All calls share it and it keeps the previous call's contents; the
+// one word that must start at zero (the decode's work counter) is cleared on
+// the stream by every call, and every partial the reduce reads is written
+// earlier in the same call.  Calls whose work overlaps on the GPU (different
+// streams, or several host threads) race on it.
 #include <mutex>
 
 #include "pa_internal.h"

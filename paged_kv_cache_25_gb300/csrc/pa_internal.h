@@ -44,6 +44,7 @@ struct DecodeArgs {
     float* ws_acc;     // [B][n_q][J][d] or null
     int part_tokens;   // tokens per partition
     int max_parts;     // J: partitions of the longest possible sequence
+    unsigned* ticket;  // work counter in the workspace's control area
     unsigned* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

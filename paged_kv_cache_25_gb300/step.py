@@ -155,17 +155,23 @@ class PagedStep:
         flush()
 
     # ------------------------------------------------------------------
-    def step(self, stream=None):
-        """One pass of the hot path; all work is enqueued on `stream`."""
+    def step(self, stream=None, prefill_events=None):
+        """One pass of the hot path; all work is enqueued on `stream`.
+        prefill_events: optional (start, stop) torch.cuda.Event pair recorded
+        around the chunked-prefill kernel."""
         wl = self.wl
         pa.pa_reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache,
                                 self.new_slots, stream=stream)
         pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
                      self.context_lens, wl.scale, wl.block_size, self.workspace, stream=stream)
         if self.R:
+            if prefill_events is not None:
+                prefill_events[0].record(stream or torch.cuda.current_stream())
             pa.pa_prefill_chunk(self.p_out, self.p_q_dev, self.k_cache, self.v_cache,
                                 self.p_block_tables, self.query_start_loc, self.p_context_lens,
                                 int(self.p_chunk.max()), wl.scale, wl.block_size, stream=stream)
+            if prefill_events is not None:
+                prefill_events[1].record(stream or torch.cuda.current_stream())
 
     # ------------------------------------------------------------------ accounting
     def kv_bytes_unique(self) -> int:
