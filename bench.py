@@ -222,6 +222,8 @@ def run_ours(args, rank, world, local_rank):
     wl = inputs.get(args.workload)
     if args.batch:
         wl = dataclasses.replace(wl, batch=args.batch)
+    if args.compact_pool:
+        wl = dataclasses.replace(wl, pool="scale", pool_arg=1.5)
     st = PagedStep(wl, seed=wl.seed + rank, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
@@ -377,6 +379,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="size the pool at 1.5x the blocks needed (profiling a smaller case)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's decode batch (profiling a smaller case)")
     args = ap.parse_args()

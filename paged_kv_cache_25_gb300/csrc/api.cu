@@ -335,7 +335,7 @@ pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const v
     a.q_start = query_start_loc; a.context_lens = context_lens;
     a.num_reqs = num_reqs; a.max_q = max_query_len; a.n_q = n_q_heads; a.scale = scale;
     a.err = err;
-    cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return ok();
 }

@@ -57,6 +57,6 @@ struct PrefillArgs {
     int num_reqs; int max_q; int n_q; float scale;
     unsigned* err;
 };
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
 }  // namespace pa
