@@ -74,11 +74,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking probe of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // records PA_ERR_TIMEOUT) if it has not completed within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;      // already complete: no suspend
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -195,6 +209,36 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uin
     hi = Cvt<T>::pack(p0, p1);
     const float2 h = Cvt<T>::unpack(hi);
     lo = Cvt<T>::pack(p0 - h.x, p1 - h.y);
+}
+
+// 2^x with the SFU's approximate exp2 (flush-to-zero; relative error ~2^-22).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Splits p into hi + lo for the MMA by truncation: hi keeps the top 16 bits of
+// p's fp32 pattern (exactly representable in bf16), lo = p - hi is exact in
+// fp32 and rounded once to T.  For fp16 the split rounds hi instead.
+template <typename T>
+__device__ __forceinline__ void split_trunc(float p0, float p1, uint32_t& hi, uint32_t& lo);
+
+template <>
+__device__ __forceinline__ void split_trunc<__nv_bfloat16>(float p0, float p1, uint32_t& hi, uint32_t& lo)
+{
+    const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+    hi = __byte_perm(u0, u1, 0x7632);                    // upper halves: (p1.hi << 16) | p0.hi
+    const float r0 = p0 - __uint_as_float(u0 & 0xFFFF0000u);
+    const float r1 = p1 - __uint_as_float(u1 & 0xFFFF0000u);
+    lo = Cvt<__nv_bfloat16>::pack(r0, r1);
+}
+
+template <>
+__device__ __forceinline__ void split_trunc<__half>(float p0, float p1, uint32_t& hi, uint32_t& lo)
+{
+    split_pair<__half>(p0, p1, hi, lo);
 }
 
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }

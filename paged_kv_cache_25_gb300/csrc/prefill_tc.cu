@@ -9,13 +9,15 @@
 // CTA = (128 M rows, KV head, request).  The M rows are (position, head) pairs
 // of one GQA group, position-major, so one pass over the keys serves all the
 // query heads that share the KV head.  Keys go in tiles of 64.
-//   warp 4  : TMA producer: 16-row K and V slabs of each 64-key tile into a
-//             3-stage ring (128-byte swizzle), one block-table lookup per block;
-//   warp 5  : one thread issues the MMAs: S = Q K^T (M 128, N 64, K = d) into a
+//   warps 8, 9: TMA producers: 16-row K (warp 8) and V (warp 9) slabs of each
+//             64-key tile into their own 3-stage rings (128-byte swizzle), one
+//             block-table lookup per block;
+//   warp 10 : one thread issues the MMAs: S = Q K^T (M 128, N 64, K = d) into a
 //             double-buffered TMEM tile, then O += P V (M 128, N = d, K 64)
 //             into TMEM, signalling completion with tcgen05.commit;
-//   warps 0-3: one thread per M row: read S from TMEM, causal mask on absolute
-//             positions, online softmax in base 2 with lazy rescaling (O in TMEM
+//   warps 0-7: two threads per M row (each half of the keys and of O): read S
+//             from TMEM, causal mask on absolute positions, online softmax in
+//             base 2 with lazy rescaling (O in TMEM
 //             is rescaled only when the running max grows by more than 2^8),
 //             P written to shared memory as hi + lo bf16/fp16 halves so that P V
 //             keeps ~16 bits of P, final O / l written to global memory.
@@ -33,7 +35,9 @@ namespace pa {
 constexpr int kTcRows = 128;      // M rows per CTA
 constexpr int kTcKeys = 64;       // keys per tile
 constexpr int kTcStages = 3;      // K/V ring depth
-constexpr int kTcThreads = 192;   // 4 softmax warps + producer + MMA issuer
+constexpr int kSoftmaxWarps = 8;
+constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1, kMmaWarp = kSoftmaxWarps + 2;
+constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;   // softmax, K producer, V producer, MMA
 constexpr uint32_t kTmemCols = 256;   // S0 [0,64) S1 [64,128) O [128, 128 + d)
 
 template <typename T, int D>
@@ -42,12 +46,12 @@ struct PfLayout {
     static constexpr uint32_t kQBytes = kTcRows * D * 2;          // Q tile
     static constexpr uint32_t kPBytes = kTcRows * kTcKeys * 2;    // one of P hi / P lo
     static constexpr uint32_t kKBytes = kTcKeys * D * 2;          // K (or V) of one tile
-    static constexpr uint32_t kStageBytes = 2 * kKBytes;
     static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffPh = kOffQ + kQBytes;
-    static constexpr uint32_t kOffPl = kOffPh + kPBytes;
-    static constexpr uint32_t kOffKV = kOffPl + kPBytes;
-    static constexpr uint32_t kDynBytes = kOffKV + kTcStages * kStageBytes + 1024;
+    static constexpr uint32_t kOffP = kOffQ + kQBytes;     // 2 buffers x (P hi, P lo)
+    static constexpr uint32_t kPBuf = 2 * kPBytes;
+    static constexpr uint32_t kOffK = kOffP + 2 * kPBuf;        // K ring
+    static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
+    static constexpr uint32_t kDynBytes = kOffV + kTcStages * kKBytes + 1024;
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -112,8 +116,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int last_row = min(rows_total, row0 + kTcRows) - 1;
     const int n_tiles = (ctx0 + last_row / group) / kTcKeys + 1;
 
-    __shared__ __align__(8) uint64_t kv_full[kTcStages], kv_empty[kTcStages];
-    __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full, pv_done, q_ready;
+    __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages];
+    __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
+    __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_ready;
+    __shared__ __align__(8) uint64_t pair_bar[4];
+    __shared__ float xmax[2][2][kTcRows];
+    __shared__ float xl[2][kTcRows];
     __shared__ uint32_t s_tmem;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -123,18 +131,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < kTcStages; ++i) {
-            mbar_init(smem_u32(&kv_full[i]), 1);
-            mbar_init(smem_u32(&kv_empty[i]), 1);
+            mbar_init(smem_u32(&k_full[i]), 1);
+            mbar_init(smem_u32(&k_empty[i]), 1);
+            mbar_init(smem_u32(&v_full[i]), 1);
+            mbar_init(smem_u32(&v_empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&s_empty[i]), 4);
+            mbar_init(smem_u32(&s_empty[i]), kSoftmaxWarps);
         }
-        mbar_init(smem_u32(&p_full), 4);
-        mbar_init(smem_u32(&pv_done), 1);
-        mbar_init(smem_u32(&q_ready), 4);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&pair_bar[i]), 2);
+        mbar_init(smem_u32(&p_full[0]), kSoftmaxWarps);
+        mbar_init(smem_u32(&p_full[1]), kSoftmaxWarps);
+        mbar_init(smem_u32(&pv_done[0]), 1);
+        mbar_init(smem_u32(&pv_done[1]), 1);
+        mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
@@ -144,20 +157,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp == 4) {
-        // ------------------------------------------------ TMA producer
+    if (warp == kKWarp || warp == kVWarp) {
+        // ------------------------------------------------ TMA producers
+        // K and V have separate rings: K of tile j is released as soon as
+        // S_j = Q K_j^T is done, V of tile j once P_j V_j is done, so each ring
+        // can run kTcStages tiles ahead of its consumer.
         if (lane == 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
+            const bool is_k = warp == kKWarp;
+            const CUtensorMap* map = is_k ? &kmap : &vmap;
+            uint64_t* full_bar = is_k ? k_full : v_full;
+            uint64_t* empty_bar = is_k ? k_empty : v_empty;
+            const uint32_t ring_base = sbase + (is_k ? Ly::kOffK : Ly::kOffV);
+            prefetch_tensormap(map);
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kTcStages;
                 if (j >= kTcStages &&
-                    !mbar_wait(smem_u32(&kv_empty[st]), ((j / kTcStages) - 1) & 1, err))
+                    !mbar_wait(smem_u32(&empty_bar[st]), ((j / kTcStages) - 1) & 1, err))
                     break;
-                const uint32_t full = smem_u32(&kv_full[st]);
-                const uint32_t kdst = sbase + Ly::kOffKV + st * Ly::kStageBytes;
-                const uint32_t vdst = kdst + Ly::kKBytes;
-                mbar_arrive_expect_tx(full, Ly::kStageBytes);
+                const uint32_t full = smem_u32(&full_bar[st]);
+                const uint32_t dst = ring_base + st * Ly::kKBytes;
+                mbar_arrive_expect_tx(full, Ly::kKBytes);
                 int b = 0;
 #pragma unroll
                 for (int c = 0; c < kTcKeys / 16; ++c) {
@@ -172,69 +191,92 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     }
                     const int row = (b * n_kv + kvh) * BS + (key0 % BS);
 #pragma unroll
-                    for (int hx = 0; hx < Ly::kHalves; ++hx) {
-                        tma_load_2d(kdst + hx * (kTcKeys * 128) + c * 2048, &kmap, hx * 64, row, full);
-                        tma_load_2d(vdst + hx * (kTcKeys * 128) + c * 2048, &vmap, hx * 64, row, full);
-                    }
+                    for (int hx = 0; hx < Ly::kHalves; ++hx)
+                        tma_load_2d(dst + hx * (kTcKeys * 128) + c * 2048, map, hx * 64, row, full);
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
+        // Descriptors are built once; each MMA only adds a constant to the
+        // start-address field (16-byte units; every operand lies below 256 KB).
         if (lane == 0) {
+            const uint64_t dq = sdesc_sw128(sbase + Ly::kOffQ, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sbase + Ly::kOffK, 16, 1024);
+            const uint64_t dp = sdesc_sw128(sbase + Ly::kOffP, 16, 1024);
+            const uint64_t dv = sdesc_sw128(sbase + Ly::kOffV, kTcKeys * 128, 1024);
+            constexpr uint32_t kQHalf = (kTcRows * 128) >> 4, kKHalf = (kTcKeys * 128) >> 4;
+            constexpr uint32_t kKStage = Ly::kKBytes >> 4, kPBufU = Ly::kPBuf >> 4;
+            constexpr uint32_t kPLo = Ly::kPBytes >> 4;
+            const uint32_t d_o = tmem + 128;
             bool ok = mbar_wait(smem_u32(&q_ready), 0, err);
             tc_fence_after();
             for (int j = 0; ok && j <= n_tiles; ++j) {
                 if (j < n_tiles) {
                     const int st = j % kTcStages, sb = j & 1;
-                    if (!mbar_wait(smem_u32(&kv_full[st]), (j / kTcStages) & 1, err)) break;
+                    if (!mbar_wait(smem_u32(&k_full[st]), (j / kTcStages) & 1, err)) break;
                     if (j >= 2 && !mbar_wait(smem_u32(&s_empty[sb]), ((j >> 1) - 1) & 1, err)) break;
                     tc_fence_after();
-                    const uint32_t kbase = sbase + Ly::kOffKV + st * Ly::kStageBytes;
+                    const uint64_t dks = dk + st * kKStage;
+                    const uint32_t d_s = tmem + sb * kTcKeys;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk & 3) * 32u;   // 16 columns = 32 bytes
-                        const uint64_t a = sdesc_sw128(sbase + Ly::kOffQ + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
-                        const uint64_t b = sdesc_sw128(kbase + (kk >> 2) * (kTcKeys * 128) + off, 16, 1024);
-                        umma_f16(tmem + sb * kTcKeys, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+                        const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
+                        const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
+                        umma_f16(d_s, dq + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(smem_u32(&s_full[sb]));
+                    umma_commit(smem_u32(&k_empty[st]));
                 }
                 if (j >= 1) {
                     const int jp = j - 1, stp = jp % kTcStages;
-                    if (!mbar_wait(smem_u32(&p_full), jp & 1, err)) break;
+                    if (!mbar_wait(smem_u32(&p_full[jp & 1]), (jp >> 1) & 1, err)) break;
+                    if (!mbar_wait(smem_u32(&v_full[stp]), (jp / kTcStages) & 1, err)) break;
                     tc_fence_after();
-                    const uint32_t vbase = sbase + Ly::kOffKV + stp * Ly::kStageBytes + Ly::kKBytes;
+                    const uint64_t dps = dp + (jp & 1) * kPBufU;
+                    const uint64_t dvs = dv + stp * kKStage;
 #pragma unroll
                     for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-                        const uint64_t ah = sdesc_sw128(sbase + Ly::kOffPh + ks * 32, 16, 1024);
-                        const uint64_t al = sdesc_sw128(sbase + Ly::kOffPl + ks * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(vbase + ks * 2048, kTcKeys * 128, 1024);
-                        umma_f16(tmem + 128, ah, b, kIdescPV, (jp > 0 || ks > 0) ? 1u : 0u);
-                        umma_f16(tmem + 128, al, b, kIdescPV, 1u);
+                        umma_f16(d_o, dps + ks * 2, dvs + ks * (2048 >> 4), kIdescPV,
+                                 (jp > 0 || ks > 0) ? 1u : 0u);
+                        umma_f16(d_o, dps + kPLo + ks * 2, dvs + ks * (2048 >> 4), kIdescPV, 1u);
                     }
-                    umma_commit(smem_u32(&pv_done));
-                    umma_commit(smem_u32(&kv_empty[stp]));
+                    umma_commit(smem_u32(&pv_done[jp & 1]));
+                    umma_commit(smem_u32(&v_empty[stp]));
                 }
             }
         }
     } else {
-        // ------------------------------------------------ softmax warps 0-3
-        const int rr = tid;                           // M row = TMEM lane
+        // ------------------------------------------------ softmax warps 0-7
+        // Warp w reads TMEM lanes 32*(w % 4) .. +31 (its M rows) and handles
+        // half (w / 4) of every tile's 64 keys and of the O columns; the two
+        // warps sharing rows swap their partial row maxima through shared
+        // memory and a two-arrival mbarrier (a bounded wait).
+        const int quarter = warp & 3, half = warp >> 2;
+        const int rr = quarter * 32 + lane;                 // M row = TMEM lane
         const int grow = row0 + rr;
         const bool valid = grow < rows_total;
         const int pos_local = valid ? grow / group : 0;
         const int head = kvh * group + (valid ? grow - (grow / group) * group : 0);
         const int p_abs = valid ? ctx0 + pos_local : L - 1;   // padding rows see every key
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t xbar = smem_u32(&pair_bar[quarter]);
+        constexpr int kHalfKeys = kTcKeys / 2;
+        constexpr int kHalfD = D / 2;
 
-        // Q row -> shared memory, 128-byte swizzled rows, one 64-column half at a time
+        // Q row -> shared memory, 128-byte swizzled rows (each warp of the pair
+        // writes half of the row).  A negative scale is applied as -Q and
+        // |scale| (an exact sign flip), so the raw-score max is the scaled max.
+        const uint32_t qsign = scale_log2 < 0.f ? 0x80008000u : 0u;
+        scale_log2 = fabsf(scale_log2);
         {
             const uint4* qp = reinterpret_cast<const uint4*>(
                 q + (static_cast<int64_t>(qs + pos_local) * n_q + head) * D);
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = valid ? __ldg(qp + c) : make_uint4(0, 0, 0, 0);
+            for (int cc = 0; cc < D / 16; ++cc) {
+                const int c = half * (D / 16) + cc;
+                uint4 v = valid ? __ldg(qp + c) : make_uint4(0, 0, 0, 0);
+                v.x ^= qsign; v.y ^= qsign; v.z ^= qsign; v.w ^= qsign;
                 const uint32_t addr = sbase + Ly::kOffQ + (c >> 3) * (kTcRows * 128) + rr * 128 +
                                       (((c & 7) ^ (rr & 7)) << 4);
                 st_shared_v4(addr, v.x, v.y, v.z, v.w);
@@ -244,9 +286,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (lane == 0) mbar_arrive(smem_u32(&q_ready));
         }
 
-        float m_used = -INFINITY, l = 0.f;
+        // smallest query position of this warp's rows (rows are position-major)
+        const int wrow = row0 + quarter * 32;
+        const int warp_min_pos = wrow < rows_total ? ctx0 + wrow / group : L - 1;
+        float m_raw = -INFINITY, l = 0.f;
         bool broken = false;
-        for (int j = 0; j < n_tiles; ++j) {
+        int j = 0;
+        for (; j < n_tiles; ++j) {
             const int sb = j & 1;
             const bool ok = mbar_wait(smem_u32(&s_full[sb]), (j >> 1) & 1, err);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -254,104 +300,155 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 break;
             }
             tc_fence_after();
-            uint32_t sr[64];
-            {
-                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                tmem_ld32(lane_addr + sb * kTcKeys, lo);
-                tmem_ld32(lane_addr + sb * kTcKeys + 32, hi);
-                tmem_ld_wait();
-            }
+            uint32_t sr[kHalfKeys];
+            tmem_ld32(lane_addr + sb * kTcKeys + half * kHalfKeys, sr);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
 
-            const int key0 = j * kTcKeys;
-            float mx = -INFINITY;
+            // scores stay raw (unscaled) until the exponent: the max is taken on
+            // raw values and p = 2^(s*c - m*c) is one FFMA and one EX2
+            const int key0 = j * kTcKeys + half * kHalfKeys;
+            const bool full_tile = key0 + kHalfKeys - 1 <= warp_min_pos;
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (full_tile) {
 #pragma unroll
-            for (int i = 0; i < kTcKeys; ++i) {
-                const float z = (key0 + i <= p_abs) ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
-                sr[i] = __float_as_uint(z);
-                mx = fmaxf(mx, z);
+                for (int i = 0; i < kHalfKeys; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < kHalfKeys; ++i) {
+                    const float z = (key0 + i <= p_abs) ? __uint_as_float(sr[i]) : -INFINITY;
+                    sr[i] = __float_as_uint(z);
+                    m4[i & 3] = fmaxf(m4[i & 3], z);
+                }
             }
-            const bool resc = mx > m_used + 8.f;      // lazy: only when the max grew a lot
+            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            // swap partial maxima with the partner warp (exchange number j)
+            xmax[j & 1][half][rr] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xbar);
+            const bool okx = mbar_wait(xbar, j & 1, err);
+            if (!__all_sync(0xffffffffu, okx)) {
+                broken = true;
+                break;
+            }
+            mx = fmaxf(mx, xmax[j & 1][half ^ 1][rr]);
+
+            // lazy: move the reference max only when the first tile sets it or
+            // the max grew by more than 2^8 (written so that scale 0 stays finite)
+            const bool first = m_raw == -INFINITY;
+            const bool resc = first ? (mx > -INFINITY) : ((mx - m_raw) * scale_log2 > 8.f);
             float fac = 1.f;
             if (resc) {
-                fac = exp2f(m_used - mx);
-                m_used = mx;
+                fac = first ? 0.f : fast_exp2((m_raw - mx) * scale_log2);
+                m_raw = mx;
                 l *= fac;
             }
-            uint32_t ph[kTcKeys / 2], pl[kTcKeys / 2];
-            float ps = 0.f;
+            const float neg_mc = -m_raw * scale_log2;
+            uint32_t ph[kHalfKeys / 2], pl[kHalfKeys / 2];
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            if (full_tile) {
 #pragma unroll
-            for (int i = 0; i < kTcKeys / 2; ++i) {
-                const float p0 = exp2f(__uint_as_float(sr[2 * i]) - m_used);
-                const float p1 = exp2f(__uint_as_float(sr[2 * i + 1]) - m_used);
-                ps += p0 + p1;
-                split_pair<T>(p0, p1, ph[i], pl[i]);
+                for (int i = 0; i < kHalfKeys / 2; ++i) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
+                    s4[i & 3] += p0 + p1;
+                    split_trunc<T>(p0, p1, ph[i], pl[i]);
+                }
+            } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
+#pragma unroll
+                for (int i = 0; i < kHalfKeys / 2; ++i) {
+                    const float s0 = __uint_as_float(sr[2 * i]), s1 = __uint_as_float(sr[2 * i + 1]);
+                    const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(fmaf(s0, scale_log2, neg_mc));
+                    const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(fmaf(s1, scale_log2, neg_mc));
+                    s4[i & 3] += p0 + p1;
+                    split_trunc<T>(p0, p1, ph[i], pl[i]);
+                }
             }
-            l += ps;
+            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
 
-            if (j >= 1) {   // the previous P V is done: P buffer free, O stable
-                const bool ok2 = mbar_wait(smem_u32(&pv_done), (j - 1) & 1, err);
+            // O is rescaled only when the reference max moved: that needs the
+            // previous P V finished (no MMA writes O while it is rescaled)
+            if (j >= 1 && __any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
+                const bool ok2 = mbar_wait(smem_u32(&pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, err);
                 if (!__all_sync(0xffffffffu, ok2)) {
                     broken = true;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_addr + 128 + c0, o);
-                        tmem_ld_wait();
+                for (int c0 = 0; c0 < kHalfD; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + 128 + half * kHalfD + c0, o);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
-                        tmem_st32(lane_addr + 128 + c0, o);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
+                    tmem_st32(lane_addr + 128 + half * kHalfD + c0, o);
+                }
+                tmem_st_wait();
+            }
+            // P buffer (j & 1) is free once the P V of tile j - 2 is done
+            if (j >= 2) {
+                const bool ok3 = mbar_wait(smem_u32(&pv_done[j & 1]), ((j - 2) >> 1) & 1, err);
+                if (!__all_sync(0xffffffffu, ok3)) {
+                    broken = true;
+                    break;
                 }
             }
+            const uint32_t pbuf = sbase + Ly::kOffP + (j & 1) * Ly::kPBuf;
 #pragma unroll
-            for (int c = 0; c < kTcKeys / 8; ++c) {
+            for (int cc = 0; cc < kHalfKeys / 8; ++cc) {
+                const int c = half * (kHalfKeys / 8) + cc;
                 const uint32_t sw = ((c ^ (rr & 7)) << 4);
-                st_shared_v4(sbase + Ly::kOffPh + rr * 128 + sw, ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-                st_shared_v4(sbase + Ly::kOffPl + rr * 128 + sw, pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+                st_shared_v4(pbuf + rr * 128 + sw, ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
+                st_shared_v4(pbuf + Ly::kPBytes + rr * 128 + sw, pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
             }
-            if (key0 + kTcKeys > L) {
+            const int tkey0 = j * kTcKeys;
+            if (tkey0 + kTcKeys > L) {
                 // keys at or past L (only in the request's last tile) may hold
-                // anything, even NaN: zero those V rows so P = 0 keeps them out
-                const int valid_rows = max(0, L - key0);
-                const int n16 = (kTcKeys - valid_rows) * 8 * Ly::kHalves;   // 16-byte pieces
-                const uint32_t vb = sbase + Ly::kOffKV + (j % kTcStages) * Ly::kStageBytes + Ly::kKBytes;
-                for (int i = tid; i < n16; i += 128) {
-                    const int hx = i / ((kTcKeys - valid_rows) * 8);
-                    const int rem = i - hx * ((kTcKeys - valid_rows) * 8);
+                // anything, even NaN: zero those V rows so P = 0 keeps them out,
+                // after the tile's V has landed
+                const bool okv = mbar_wait(smem_u32(&v_full[j % kTcStages]), (j / kTcStages) & 1, err);
+                if (!__all_sync(0xffffffffu, okv)) {
+                    broken = true;
+                    break;
+                }
+                const int valid_rows = max(0, L - tkey0);
+                const int per_half = (kTcKeys - valid_rows) * 8;      // 16-byte pieces
+                const uint32_t vb = sbase + Ly::kOffV + (j % kTcStages) * Ly::kKBytes;
+                for (int i = tid; i < per_half * Ly::kHalves; i += 8 * 32) {
+                    const int hx = i / per_half;
+                    const int rem = i - hx * per_half;
                     st_shared_v4(vb + hx * (kTcKeys * 128) + valid_rows * 128 + rem * 16, 0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
         }
 
         // ------------------------------------------------ epilogue: O / l
         if (!broken) {
-            const bool ok = mbar_wait(smem_u32(&pv_done), (n_tiles - 1) & 1, err);
-            if (__all_sync(0xffffffffu, ok)) {
+            xl[half][rr] = l;                   // swap partial sums (exchange n_tiles)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xbar);
+            const bool okx = mbar_wait(xbar, n_tiles & 1, err);
+            const bool ok = mbar_wait(smem_u32(&pv_done[(n_tiles - 1) & 1]), ((n_tiles - 1) >> 1) & 1, err);
+            if (__all_sync(0xffffffffu, ok && okx)) {
                 tc_fence_after();
-                const float inv = 1.f / l;
+                const float inv = 1.f / (l + xl[half ^ 1][rr]);
                 const int64_t obase = (static_cast<int64_t>(qs + pos_local) * n_q + head) * D;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < kHalfD; c0 += 32) {
                     uint32_t o[32];
-                    tmem_ld32(lane_addr + 128 + c0, o);
+                    tmem_ld32(lane_addr + 128 + half * kHalfD + c0, o);
                     tmem_ld_wait();
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv;
-                    if (valid) store_row<T>(out, obase, c0, v, 32, out_dtype);
+                    if (valid) store_row<T>(out, obase, half * kHalfD + c0, v, 32, out_dtype);
                 }
             }
         }
@@ -360,7 +457,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <typename T, int D, int BS>

@@ -99,3 +99,32 @@ def test_prefill_mixed_workload_sampled_rows():
         got = st.p_out[int(qsl[r]) + np.array(rows)]
         assert max_err(got, ref) <= 2e-3
     assert torch.isfinite(st.p_out).all()
+
+
+def test_prefill_negative_and_zero_scale():
+    """The kernel takes the max on raw scores; a negative scale must flip it."""
+    import torch
+    for scale in (-0.09, 0.0):
+        d, bs, n_q, n_kv = 64, 16, 8, 2
+        rng = np.random.default_rng(5)
+        L, C = 90, 40
+        nb = 10
+        alloc = pa.Allocator(nb, rng.permutation(nb).astype(np.int32))
+        tables = alloc.build_tables([L], 6, bs)
+        g = torch.Generator().manual_seed(3)
+        k = torch.randn(L, n_kv, d, generator=g).to(torch.bfloat16)
+        v = torch.randn(L, n_kv, d, generator=g).to(torch.bfloat16)
+        qq = torch.randn(C, n_q, d, generator=g).to(torch.bfloat16)
+        kc = torch.full((nb, n_kv, bs, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        vc = kc.clone()
+        slots = torch.from_numpy(pa.pa_slot_mapping(tables, bs, np.zeros(L, np.int32),
+                                                    np.arange(L, dtype=np.int32))).cuda()
+        pa.pa_reshape_and_cache(k.cuda(), v.cuda(), kc, vc, slots)
+        out = torch.empty((C, n_q, d), dtype=torch.float32, device="cuda")
+        pa.pa_prefill_chunk(out, qq.cuda(), kc, vc, torch.from_numpy(tables).cuda(),
+                            torch.tensor([0, C], dtype=torch.int32, device="cuda"),
+                            torch.tensor([L], dtype=torch.int32, device="cuda"), C, scale, bs)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0
+        ref = oracle.prefill([qq], [k], [v], float(np.float32(scale)))[0]
+        assert max_err(out, ref) <= 2e-3
