@@ -175,6 +175,33 @@ pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q,
 
 size_t pa_prefill_workspace_size(int num_reqs, int n_q_heads, int head_dim, int total_q);
 
+/* ---------------------------------------------------------------- block copies
+ * Copy-on-write ("vLLM Serving ...", "Sharing and copy-on-write": a sharer
+ * that diverges gets a copy of the one shared block it writes to, then its
+ * block table points at the copy).  For i < num_pairs, every K and V row of
+ * physical block block_mapping[2i] (all KV heads) is copied over block
+ * block_mapping[2i+1] of the same pools.
+ *   block_mapping : int32 [num_pairs][2] (source, destination), device-readable.
+ * Every source block is read as it was before the call; a destination must not
+ * also be a source in the same call (the copies run in parallel).  An id
+ * outside [0, num_blocks) sets PA_ERR_OUT_OF_RANGE on the device and that pair
+ * is skipped. */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc* cache,
+                         const int32_t* block_mapping, int num_pairs, void* stream);
+
+/* Swap ("vLLM Serving ...", "The scheduler: waiting, running, swapped": the
+ * blocks of a preempted sequence move to a pool in CPU memory and come back
+ * when it resumes).  Copies whole blocks from one pool pair to another of the
+ * same layout (layout->num_blocks is ignored; the two sizes are given).  Either
+ * side may be device memory or page-locked host memory mapped into the GPU's
+ * address space (cudaHostAlloc / cudaMallocHost, or registered as mapped), so
+ * one call moves many blocks with no per-block cudaMemcpy.  Same mapping rules
+ * as pa_copy_blocks; ids are checked against each side's block count. */
+pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks,
+                         void* dst_k, void* dst_v, int dst_num_blocks,
+                         const pa_cache_desc* layout, const int32_t* block_mapping,
+                         int num_pairs, void* stream);
+
 /* ---------------------------------------------------------------- errors
  * Synchronizes `stream`, returns the device error word (PA_OK if clean) and
  * clears it.  The word is per device and shared by every stream. */

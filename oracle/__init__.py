@@ -64,6 +64,7 @@ def _load():
                 "orc_slot_mapping": (None, [P, I, I, P, P, I, P]),
                 "orc_cache_write": (None, [P, P, P, P, P, I, I, I, I, I, I]),
                 "orc_gather": (None, [P, P, I, I, I, I, I, P]),
+                "orc_copy_blocks": (None, [P, P, P, P, P, I, L]),
                 "orc_decode": (None, [P, P, P, P, P, P, I, I, I, I, D, I]),
                 "orc_prefill": (None, [P, P, P, P, P, P, P, P, I, I, I, I, D, I]),
             }
@@ -193,6 +194,18 @@ def cache_write(k_cache, v_cache, k, v, slots, block_size: int):
     _load().orc_cache_write(_ptr(kc), _ptr(vc), _ptr(kb), _ptr(vb), _ptr(slots), len(slots),
                             NB, n_kv, bs, d, eb)
     return kc, vc
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, mapping):
+    """Returns new (dst_k, dst_v) byte arrays: whole blocks mapping[i][0] of
+    the source pools copied over blocks mapping[i][1] of the destination."""
+    NB, n_kv, bs, d = src_k.shape
+    bb = n_kv * bs * d * src_k.element_size()
+    sk, sv = _bytes(src_k), _bytes(src_v)
+    dk, dv = _bytes(dst_k), _bytes(dst_v)
+    m = _c(mapping, np.int32).reshape(-1, 2)
+    _load().orc_copy_blocks(_ptr(sk), _ptr(sv), _ptr(dk), _ptr(dv), _ptr(m), len(m), bb)
+    return dk, dv
 
 
 def gather(cache, table, L: int) -> np.ndarray:

@@ -158,6 +158,16 @@ void orc_cache_write(uint8_t* k_cache, uint8_t* v_cache, const uint8_t* k, const
     }
 }
 
+void orc_copy_blocks(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k, uint8_t* dst_v,
+                     const int32_t* map, int n, int64_t block_bytes)
+{
+    for (int i = 0; i < n; ++i) {
+        int64_t s = map[2 * i], d = map[2 * i + 1];
+        memmove(dst_k + d * block_bytes, src_k + s * block_bytes, (size_t)block_bytes);
+        memmove(dst_v + d * block_bytes, src_v + s * block_bytes, (size_t)block_bytes);
+    }
+}
+
 void orc_gather(const uint8_t* cache, const int32_t* table, int L, int n_kv, int block_size,
                 int head_dim, int elem_bytes, uint8_t* out)
 {

@@ -16,7 +16,10 @@
  *              proper" (free block queue, page table, a new block every 16
  *              tokens, blocks returned immediately)
  *   [Sharing]  "vLLM Serving ...", "Sharing and copy-on-write" (several
- *              block tables point at one physical block; reference counts)
+ *              block tables point at one physical block; reference counts;
+ *              a sharer that diverges gets a copy of that one block) and
+ *              "The scheduler: waiting, running, swapped" (blocks of preempted
+ *              sequences move to CPU memory and back)
  *   [Detour]   "Life of a prompt", sections "The detour, what really happens
  *              inside one forward pass" and "The decode stage" (softmax of
  *              Q K^T, times V; one query row per decode step; K/V appended)
@@ -70,6 +73,16 @@ void orc_slot_mapping(const int32_t* tables, int max_blocks, int block_size,
 void orc_cache_write(uint8_t* k_cache, uint8_t* v_cache, const uint8_t* k, const uint8_t* v,
                      const int64_t* slots, int T, int num_blocks, int n_kv, int block_size,
                      int head_dim, int elem_bytes);
+
+/* [Sharing] copy-on-write / swap: for i < n, copy the whole physical block
+ * map[i][0] of the source pools (all KV heads, all rows, K and V) over block
+ * map[i][1] of the destination pools.  Every source block is read as it was
+ * before the call (callers pass copies of the source pools), so the order of
+ * the pairs does not matter; a destination must not also be a source of the
+ * same call when the pools are the same.
+ * block_bytes = n_kv * block_size * head_dim * elem_bytes. */
+void orc_copy_blocks(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k, uint8_t* dst_v,
+                     const int32_t* map, int n, int64_t block_bytes);
 
 /* [Kernel] logical row p of a sequence lives in block table[p / bs], offset
  * p % bs; copy rows 0..L-1 out as a contiguous [L][n_kv][d] array. */

@@ -20,7 +20,7 @@ __all__ = [
     "PAError", "lib", "pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_size",
     "pa_decode_no_alloc", "PA_DECODE_NO_ALLOC_SCRATCH_BYTES",
     "pa_prefill_chunk", "pa_prefill_workspace_size", "pa_get_device_error", "pa_status_string",
-    "pa_set_profile_events", "Allocator", "pa_slot_mapping", "pa_kv_bytes_per_token",
+    "pa_set_profile_events", "pa_copy_blocks", "pa_swap_blocks", "Allocator", "pa_slot_mapping", "pa_kv_bytes_per_token",
     "pa_pool_blocks", "EXPORTED", "dtype_code",
 ]
 
@@ -42,6 +42,8 @@ _SIGS = {
     "pa_decode_no_alloc": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, F, I, P]),
     "pa_prefill_chunk": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, P, I, I, I, F, I, P, SZ, P]),
     "pa_prefill_workspace_size": (SZ, [I, I, I, I]),
+    "pa_copy_blocks": (I, [P, P, C.POINTER(_Desc), P, I, P]),
+    "pa_swap_blocks": (I, [P, P, I, P, P, I, C.POINTER(_Desc), P, I, P]),
     "pa_get_device_error": (I, [P]),
     "pa_status_string": (C.c_char_p, [I]),
     "pa_last_error_message": (C.c_char_p, []),
@@ -190,6 +192,22 @@ def pa_prefill_chunk(out, q, k_cache, v_cache, block_tables, query_start_loc, co
                                   _ptr(context_lens), R, int(max_query_len), n_q, float(scale),
                                   int(block_size), _ptr(workspace), ws_bytes, _stream(stream)),
            "pa_prefill_chunk")
+
+
+def pa_copy_blocks(k_cache, v_cache, block_mapping, stream=None):
+    """Copy whole blocks mapping[i][0] -> mapping[i][1] within the pools."""
+    d = _desc(k_cache)
+    _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), C.byref(d), _ptr(block_mapping),
+                                int(block_mapping.shape[0]), _stream(stream)), "pa_copy_blocks")
+
+
+def pa_swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, stream=None):
+    """Copy whole blocks between two pools of one layout; either side may be a
+    pinned host tensor (torch pin_memory) or a device tensor."""
+    d = _desc(src_k)
+    _check(lib().pa_swap_blocks(_ptr(src_k), _ptr(src_v), int(src_k.shape[0]), _ptr(dst_k),
+                                _ptr(dst_v), int(dst_k.shape[0]), C.byref(d), _ptr(block_mapping),
+                                int(block_mapping.shape[0]), _stream(stream)), "pa_swap_blocks")
 
 
 def pa_get_device_error(stream=None) -> int:

@@ -218,6 +218,41 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
     return ok();
 }
 
+pa_status pa_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks, void* dst_k,
+                         void* dst_v, int dst_num_blocks, const pa_cache_desc* layout,
+                         const int32_t* block_mapping, int num_pairs, void* stream)
+{
+    if (!layout) return fail(PA_ERR_INVALID_ARG, "layout descriptor is NULL");
+    pa_cache_desc c = *layout;
+    c.num_blocks = src_num_blocks > 0 ? src_num_blocks : 1;
+    pa_status st = check_cache(&c);
+    if (st != PA_OK) return st;
+    if (num_pairs < 0 || src_num_blocks < 0 || dst_num_blocks < 0)
+        return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_pairs == 0) return ok();
+    if (num_pairs > 65535) return fail(PA_ERR_UNSUPPORTED, "more than 65535 block pairs per call");
+    if (!src_k || !src_v || !dst_k || !dst_v || !block_mapping)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v) ||
+        (reinterpret_cast<uintptr_t>(block_mapping) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARG, "pools must be 16-byte and the mapping 8-byte aligned");
+    unsigned* err = device_error_word();
+    if (!err) return fail(PA_ERR_CUDA, "cannot locate the device error word");
+    cudaError_t e = launch_copy_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v, dst_num_blocks,
+                                       *layout, block_mapping, num_pairs, err,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+    return ok();
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc* cache,
+                         const int32_t* block_mapping, int num_pairs, void* stream)
+{
+    if (!cache) return fail(PA_ERR_INVALID_ARG, "cache descriptor is NULL");
+    return pa_swap_blocks(k_cache, v_cache, cache->num_blocks, k_cache, v_cache, cache->num_blocks,
+                          cache, block_mapping, num_pairs, stream);
+}
+
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
                                 int block_size, int max_context_len)
 {

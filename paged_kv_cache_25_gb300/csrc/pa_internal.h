@@ -35,6 +35,10 @@ cudaError_t launch_cache_write(const void* k, const void* v, void* kc, void* vc,
                                const int64_t* slots, int T, const pa_cache_desc& c,
                                unsigned* err, cudaStream_t s);
 
+cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, int src_blocks, void* dst_k,
+                               void* dst_v, int dst_blocks, const pa_cache_desc& layout,
+                               const int32_t* mapping, int pairs, unsigned* err, cudaStream_t s);
+
 struct DecodeArgs {
     void* out; pa_dtype out_dtype; const void* q;
     const void* k_cache; const void* v_cache; pa_cache_desc cache;

@@ -358,3 +358,49 @@ def test_decode_threads_do_not_change_bits():
     a = oracle.decode(dr.q(), [k for k, _ in kvs], [v for _, v in kvs], wl.scale, threads=1)
     b = oracle.decode(dr.q(), [k for k, _ in kvs], [v for _, v in kvs], wl.scale, threads=5)
     assert np.array_equal(a, b)
+
+
+def test_copy_blocks_copy_on_write_example():
+    """[Sharing] two tables share a block; the diverging sharer gets a copy of
+    that one block and its own table entry is updated; the original stays."""
+    dtype = torch.float32
+    nb, n_kv, bs, d = 6, 2, 4, 8
+    g = torch.Generator().manual_seed(0)
+    k = torch.randn(nb, n_kv, bs, d, generator=g)
+    v = torch.randn(nb, n_kv, bs, d, generator=g)
+    a = oracle.Allocator(nb, np.arange(nb))
+    shared = a.take(1)
+    a.share(shared)                       # two sequences point at block 0
+    new = a.take(1)                       # sequence B diverges: copy 0 -> 1
+    dk, dv = oracle.copy_blocks(k, v, k, v, [[int(shared[0]), int(new[0])]])
+    a.release(shared)                     # B drops its reference to the shared block
+    kk = torch.from_numpy(dk).view(dtype).reshape(k.shape)
+    vv = torch.from_numpy(dv).view(dtype).reshape(v.shape)
+    assert torch.equal(kk[1], k[0]) and torch.equal(vv[1], v[0])      # the copy
+    assert torch.equal(kk[0], k[0]) and torch.equal(kk[2:], k[2:])    # nothing else moves
+    assert a.refcount(int(shared[0])) == 1 and a.refcount(int(new[0])) == 1
+    # a copy then gathers to the same logical rows through the updated table
+    tb_a, tb_b = [int(shared[0])], [int(new[0])]
+    assert np.array_equal(oracle.gather(kk, tb_a, 3), oracle.gather(kk, tb_b, 3))
+
+
+def test_copy_blocks_swap_round_trip_and_chains():
+    nb, n_kv, bs, d = 5, 1, 2, 4
+    k = torch.arange(nb * n_kv * bs * d, dtype=torch.float32).reshape(nb, n_kv, bs, d)
+    v = -k
+    host_k = torch.zeros_like(k); host_v = torch.zeros_like(v)
+    hk, hv = oracle.copy_blocks(k, v, host_k, host_v, [[3, 0], [1, 4]])     # out to "CPU"
+    hk_t = torch.from_numpy(hk).view(torch.float32).reshape(k.shape)
+    hv_t = torch.from_numpy(hv).view(torch.float32).reshape(v.shape)
+    assert torch.equal(hk_t[0], k[3]) and torch.equal(hk_t[4], k[1]) and torch.equal(hv_t[0], v[3])
+    back_k, _ = oracle.copy_blocks(hk_t, hv_t, torch.zeros_like(k), torch.zeros_like(v), [[0, 2], [4, 0]])
+    bk = torch.from_numpy(back_k).view(torch.float32).reshape(k.shape)
+    assert torch.equal(bk[2], k[3]) and torch.equal(bk[0], k[1])
+    # every source block is read as it was before the call (copies run in
+    # parallel on the GPU), so the order of the pairs does not matter
+    m = [[0, 1], [3, 2], [4, 0]]
+    ck1, _ = oracle.copy_blocks(k, v, k, v, m)
+    ck2, _ = oracle.copy_blocks(k, v, k, v, m[::-1])
+    assert np.array_equal(ck1, ck2)
+    ckt = torch.from_numpy(ck1).view(torch.float32).reshape(k.shape)
+    assert torch.equal(ckt[1], k[0]) and torch.equal(ckt[2], k[3]) and torch.equal(ckt[0], k[4])
