@@ -65,6 +65,10 @@ def _load():
                 "orc_cache_write": (None, [P, P, P, P, P, I, I, I, I, I, I]),
                 "orc_gather": (None, [P, P, I, I, I, I, I, P]),
                 "orc_copy_blocks": (None, [P, P, P, P, P, I, L]),
+                "orc_fp8_e4m3_encode": (C.c_uint8, [C.c_float]),
+                "orc_fp8_e4m3_decode": (D, [C.c_uint8]),
+                "orc_quantize_fp8": (None, [P, L, C.c_float, P]),
+                "orc_dequantize_fp8": (None, [P, L, D, P]),
                 "orc_decode": (None, [P, P, P, P, P, P, I, I, I, I, D, I]),
                 "orc_prefill": (None, [P, P, P, P, P, P, P, P, I, I, I, I, D, I]),
             }
@@ -216,6 +220,33 @@ def gather(cache, table, L: int) -> np.ndarray:
     table = _c(table, np.int32)
     out = np.empty(L * n_kv * d * eb, np.uint8)
     _load().orc_gather(_ptr(cb), _ptr(table), L, n_kv, bs, d, eb, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- fp8 e4m3
+
+def fp8_encode(x: float) -> int:
+    return int(_load().orc_fp8_e4m3_encode(float(x)))
+
+
+def fp8_decode(code: int) -> float:
+    return float(_load().orc_fp8_e4m3_decode(int(code)))
+
+
+def quantize_fp8(x, scale: float) -> np.ndarray:
+    """uint8 codes of encode(fp32(x) / fp32(scale)), same shape as x."""
+    import torch
+    xf = x.detach().cpu().to(torch.float32).numpy() if isinstance(x, torch.Tensor) else np.asarray(x, np.float32)
+    xf = np.ascontiguousarray(xf, np.float32)
+    out = np.empty(xf.shape, np.uint8)
+    _load().orc_quantize_fp8(_ptr(xf), xf.size, float(scale), _ptr(out))
+    return out
+
+
+def dequantize_fp8(codes, scale: float) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes), np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().orc_dequantize_fp8(_ptr(c), c.size, float(np.float32(scale)), _ptr(out))
     return out
 
 

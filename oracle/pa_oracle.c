@@ -181,6 +181,51 @@ void orc_gather(const uint8_t* cache, const int32_t* table, int L, int n_kv, int
     }
 }
 
+/* ------------------------------------------------------------ fp8 e4m3 */
+
+double orc_fp8_e4m3_decode(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 0xF, m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);          /* subnormal: m/8 * 2^(1-7) */
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+uint8_t orc_fp8_e4m3_encode(float xf)
+{
+    double x = (double)xf;
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = x < 0 ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);        /* saturate */
+    /* nearest of the 127 non-negative finite codes, ties to the even code */
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(orc_fp8_e4m3_decode((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void orc_quantize_fp8(const float* x, int64_t n, float scale, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float q = x[i] / scale;                            /* fp32 division */
+        out[i] = orc_fp8_e4m3_encode(q);
+    }
+}
+
+void orc_dequantize_fp8(const uint8_t* code, int64_t n, double scale, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_fp8_e4m3_decode(code[i]) * scale;
+}
+
 /* -------------------------------------------------------------- attention */
 
 /* One query row against rows 0..n-1 of one K/V head:

@@ -28,6 +28,9 @@
  *              attention as over a contiguous tensor)
  *   [Chunked]  "The hands-on guide to LLM Inference with vLLM", chunked
  *              prefill: each chunk attends to every earlier cached token
+ *   [Quant]    same guide, KV cache footprint ("1 if you quantize the cache
+ *              to FP8") and "vLLM Serving ...", quantization (--kv-cache-dtype
+ *              fp8 roughly doubles KV capacity)
  *
  * Values are read as their stored numbers converted exactly to double.
  */
@@ -83,6 +86,16 @@ void orc_cache_write(uint8_t* k_cache, uint8_t* v_cache, const uint8_t* k, const
  * block_bytes = n_kv * block_size * head_dim * elem_bytes. */
 void orc_copy_blocks(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k, uint8_t* dst_v,
                      const int32_t* map, int n, int64_t block_bytes);
+
+/* [Quant] FP8 E4M3 cache: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits, subnormals, largest finite 448, no infinities, NaN = all exponent and
+ * mantissa bits set.  Encoding rounds to nearest, ties to even, and saturates
+ * to +-448.  A cache value is encode(x / scale) with the division in fp32;
+ * its meaning is decode(code) * scale. */
+uint8_t orc_fp8_e4m3_encode(float x);
+double  orc_fp8_e4m3_decode(uint8_t code);
+void    orc_quantize_fp8(const float* x, int64_t n, float scale, uint8_t* out);
+void    orc_dequantize_fp8(const uint8_t* code, int64_t n, double scale, double* out);
 
 /* [Kernel] logical row p of a sequence lives in block table[p / bs], offset
  * p % bs; copy rows 0..L-1 out as a contiguous [L][n_kv][d] array. */

@@ -404,3 +404,50 @@ def test_copy_blocks_swap_round_trip_and_chains():
     assert np.array_equal(ck1, ck2)
     ckt = torch.from_numpy(ck1).view(torch.float32).reshape(k.shape)
     assert torch.equal(ckt[1], k[0]) and torch.equal(ckt[2], k[3]) and torch.equal(ckt[0], k[4])
+
+
+# ------------------------------------------------------------- fp8 e4m3
+
+def test_fp8_e4m3_decode_known_codes():
+    """Values fixed by the E4M3 format definition (bias 7, 3 mantissa bits)."""
+    known = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x39: 1.125, 0x40: 2.0, 0x7E: 448.0, 0x7D: 416.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in known.items():
+        assert oracle.fp8_decode(c) == v, hex(c)
+    assert math.isnan(oracle.fp8_decode(0x7F)) and math.isnan(oracle.fp8_decode(0xFF))
+
+
+def test_fp8_e4m3_round_trip_monotone_ties_saturation():
+    vals = [oracle.fp8_decode(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(vals, vals[1:]))                 # strictly increasing
+    for c in list(range(0x7F)) + list(range(0x81, 0xFF)):
+        assert oracle.fp8_encode(oracle.fp8_decode(c)) == c            # exact round trip
+    assert oracle.fp8_encode(1.0625) == 0x38                           # tie -> even mantissa
+    assert oracle.fp8_encode(1.1875) == 0x3A
+    assert oracle.fp8_encode(1.07) == 0x39                             # nearest
+    assert oracle.fp8_encode(1000.0) == 0x7E and oracle.fp8_encode(-1e30) == 0xFE
+    assert oracle.fp8_encode(2.0 ** -11) == 0x00                       # below half the smallest
+    assert oracle.fp8_encode(3 * 2.0 ** -11) == 0x01                   # rounds up to 2^-9
+
+
+def test_fp8_e4m3_matches_library_cast_in_range():
+    """torch's float8_e4m3fn cast is round-to-nearest-even; compare in range."""
+    g = torch.Generator().manual_seed(1)
+    x = torch.cat([torch.randn(4000, generator=g) * 60, torch.randn(2000, generator=g) * 0.01])
+    x = x.clamp(-440, 440)
+    ours = oracle.quantize_fp8(x, 1.0)
+    lib = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, lib)
+
+
+def test_fp8_quantize_divides_in_fp32_then_rounds():
+    scale = 0.0125
+    x = torch.tensor([1.0, -3.3, 0.05, 5.0], dtype=torch.float32)     # within 448 * scale
+    codes = oracle.quantize_fp8(x, scale)
+    for xi, c in zip(x.tolist(), codes.tolist()):
+        q = np.float32(xi) / np.float32(scale)
+        assert c == oracle.fp8_encode(float(q))
+    deq = oracle.dequantize_fp8(codes, scale)
+    # relative rounding error of 3 mantissa bits is at most 2^-4
+    assert np.all(np.abs(deq - x.numpy()) <= 0.0625 * np.abs(x.numpy()) + 2.0 ** -9 * scale)
+    assert oracle.quantize_fp8(torch.tensor([9.0]), scale)[0] == 0x7E   # 720 saturates to 448
