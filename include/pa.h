@@ -58,17 +58,25 @@ typedef enum {
     PA_ERR_CUDA = 6           /* a CUDA runtime call failed                      */
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 /* Shape of one layer's paged K/V pool.  head_dim in {64, 128} and block_size
  * in {16, 32} run on the tensor-core paths; fp32 pools run on a CUDA-core
- * path.  n_kv_heads >= 1. */
+ * path.  n_kv_heads >= 1.
+ * FP8 pools ("The hands-on guide to LLM Inference with vLLM", KV footprint:
+ * 1 byte per element if the cache is quantized to FP8): dtype PA_FP8_E4M3,
+ * each stored code c means decode_e4m3(c) * k_scale for K (v_scale for V);
+ * act_dtype (PA_BF16 or PA_F16) is the dtype of q and of the K/V rows given
+ * to pa_reshape_and_cache_quant.  The three fields are ignored otherwise. */
 typedef struct {
     int num_blocks;
     int block_size;
     int n_kv_heads;
     int head_dim;
     pa_dtype dtype;
+    float k_scale;
+    float v_scale;
+    pa_dtype act_dtype;
 } pa_cache_desc;
 
 /* ---------------------------------------------------------------- cache write
@@ -85,6 +93,17 @@ typedef struct {
 pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                const int64_t* slot_mapping, int num_tokens,
                                const pa_cache_desc* cache, void* stream);
+
+/* Cache write with conversion: k, v are [num_tokens][n_kv_heads][head_dim] in
+ * in_dtype (PA_F32, PA_F16 or PA_BF16).  Into an FP8 pool each element is
+ * stored as the E4M3 code of fp32(x) / k_scale (v_scale for V), the division
+ * IEEE-rounded in fp32, the code rounded to nearest even and saturated to
+ * +-448.  Into a pool of in_dtype it is pa_reshape_and_cache.  Other pairs
+ * return PA_ERR_UNSUPPORTED.  Slot rules as for pa_reshape_and_cache. */
+pa_status pa_reshape_and_cache_quant(const void* k, const void* v, pa_dtype in_dtype,
+                                     void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int num_tokens,
+                                     const pa_cache_desc* cache, void* stream);
 
 /* ---------------------------------------------------------------- decode
  * One query row per sequence ("Life of a prompt", "The decode stage"):
@@ -110,7 +129,10 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
  *                  and, for long contexts split over several thread blocks,
  *                  the partial results the second kernel combines.  Calls that
  *                  overlap on the GPU must not share one workspace.
- * n_q_heads must be a multiple of n_kv_heads.  Accumulation is fp32. */
+ * n_q_heads must be a multiple of n_kv_heads.  Accumulation is fp32.
+ * FP8 pools: q is in cache->act_dtype; K/V codes are widened exactly to fp16
+ * and q is rounded to fp16 for the tensor-core products (exact for bf16 q of
+ * magnitude in [2^-14, 65504]); the scales multiply the scores and the output. */
 pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
                     const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
                     const int32_t* block_tables, int max_blocks_per_seq,
@@ -164,7 +186,7 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
  *                     request r including the chunk (C_r <= L_r).
  *   max_query_len   : host value >= every C_r (sizes the grid).
  *   workspace       : reserved; pass NULL / 0 (pa_prefill_workspace_size is 0).
- * bf16 and fp16 pools only. */
+ * bf16 and fp16 pools only (FP8 pools return PA_ERR_UNSUPPORTED). */
 pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q,
                            const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
                            const int32_t* block_tables, int max_blocks_per_seq,

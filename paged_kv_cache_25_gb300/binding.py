@@ -17,7 +17,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "PAError", "lib", "pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_size",
+    "PAError", "lib", "pa_reshape_and_cache", "pa_reshape_and_cache_quant", "pa_decode",
+    "pa_decode_workspace_size",
     "pa_decode_no_alloc", "PA_DECODE_NO_ALLOC_SCRATCH_BYTES",
     "pa_prefill_chunk", "pa_prefill_workspace_size", "pa_get_device_error", "pa_status_string",
     "pa_set_profile_events", "pa_copy_blocks", "pa_swap_blocks", "Allocator", "pa_slot_mapping", "pa_kv_bytes_per_token",
@@ -26,12 +27,14 @@ __all__ = [
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE = 0, 1, 2, 3
 PA_ERR_WORKSPACE, PA_ERR_TIMEOUT, PA_ERR_CUDA = 4, 5, 6
-_DT = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+_DT = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.float8_e4m3fn: 3}
+PA_FP8_E4M3 = 3
 
 
 class _Desc(C.Structure):
     _fields_ = [("num_blocks", C.c_int), ("block_size", C.c_int), ("n_kv_heads", C.c_int),
-                ("head_dim", C.c_int), ("dtype", C.c_int)]
+                ("head_dim", C.c_int), ("dtype", C.c_int), ("k_scale", C.c_float),
+                ("v_scale", C.c_float), ("act_dtype", C.c_int)]
 
 
 P, I, L, F, SZ, U8P = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t, C.c_void_p
@@ -40,6 +43,7 @@ _SIGS = {
     "pa_decode": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, F, I, P, SZ, P]),
     "pa_decode_workspace_size": (SZ, [I, I, I, I, I, I]),
     "pa_decode_no_alloc": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, F, I, P]),
+    "pa_reshape_and_cache_quant": (I, [P, P, I, P, P, P, I, C.POINTER(_Desc), P]),
     "pa_prefill_chunk": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, P, I, I, I, F, I, P, SZ, P]),
     "pa_prefill_workspace_size": (SZ, [I, I, I, I]),
     "pa_copy_blocks": (I, [P, P, C.POINTER(_Desc), P, I, P]),
@@ -120,9 +124,15 @@ def _stream(stream) -> int | None:
     return stream
 
 
-def _desc(k_cache: torch.Tensor) -> _Desc:
+def _desc(k_cache: torch.Tensor, k_scale=None, v_scale=None, act_dtype=None) -> _Desc:
+    """Cache descriptor; FP8 pools (torch.float8_e4m3fn) need the two scales and
+    the activation dtype (of q and of the rows written into the pool)."""
     nb, n_kv, bs, d = k_cache.shape
-    return _Desc(nb, bs, n_kv, d, dtype_code(k_cache.dtype))
+    dt = dtype_code(k_cache.dtype)
+    if dt == PA_FP8_E4M3:   # missing scales reach the library as 0 and are refused there
+        return _Desc(nb, bs, n_kv, d, dt, float(k_scale or 0.0), float(v_scale or 0.0),
+                     dtype_code(act_dtype) if act_dtype is not None else -1)
+    return _Desc(nb, bs, n_kv, d, dt, 1.0, 1.0, dt)
 
 
 def pa_status_string(st: int) -> str:
@@ -144,11 +154,24 @@ def pa_decode_workspace_size(num_seqs, n_q_heads, n_kv_heads, head_dim, block_si
                                               block_size, max_context_len))
 
 
+def pa_reshape_and_cache_quant(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
+                               stream=None):
+    """k, v [T][n_kv][d] (fp32/fp16/bf16) -> pools, quantized to E4M3 codes of
+    x / scale when the pools are torch.float8_e4m3fn."""
+    assert k.is_contiguous() and v.is_contiguous() and slot_mapping.dtype == torch.int64
+    d = _desc(k_cache, k_scale, v_scale, k.dtype)
+    _check(lib().pa_reshape_and_cache_quant(_ptr(k), _ptr(v), dtype_code(k.dtype), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(slot_mapping), int(k.shape[0]),
+                                            C.byref(d), _stream(stream)),
+           "pa_reshape_and_cache_quant")
+
+
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
-              block_size: int, workspace=None, stream=None):
-    """out [B][n_q][d] (fp32/fp16/bf16) = paged decode attention of q [B][n_q][d]."""
+              block_size: int, workspace=None, stream=None, k_scale=None, v_scale=None):
+    """out [B][n_q][d] (fp32/fp16/bf16) = paged decode attention of q [B][n_q][d].
+    FP8 pools also take k_scale and v_scale."""
     B, n_q, _ = q.shape
-    d = _desc(k_cache)
+    d = _desc(k_cache, k_scale, v_scale, q.dtype)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().pa_decode(_ptr(out), dtype_code(out.dtype), _ptr(q), _ptr(k_cache),
                            _ptr(v_cache), C.byref(d), _ptr(block_tables),

@@ -72,18 +72,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 pa_status encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int head_dim,
-                          uint64_t rows, int box_x, int box_y)
+                          uint64_t rows, int box_x, int box_y, bool swizzle128)
 {
     auto fn = encode_fn();
     if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const CUtensorMapDataType t =
-        dt == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+        dt == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                     : (dt == PA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16);
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elem_bytes(dt)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y)};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, t, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return PA_OK;
@@ -115,11 +117,20 @@ int decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int ma
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static pa_status check_cache(const pa_cache_desc* c)
+// need_act: the call reads q in act_dtype (decode); a cache write names its
+// input dtype itself and ignores act_dtype.
+static pa_status check_cache(const pa_cache_desc* c, bool need_act = true)
 {
     if (!c) return fail(PA_ERR_INVALID_ARG, "cache descriptor is NULL");
-    if (c->dtype != PA_F32 && c->dtype != PA_F16 && c->dtype != PA_BF16)
+    if (c->dtype != PA_F32 && c->dtype != PA_F16 && c->dtype != PA_BF16 && c->dtype != PA_FP8_E4M3)
         return fail(PA_ERR_INVALID_ARG, "unknown cache dtype %d", (int)c->dtype);
+    if (c->dtype == PA_FP8_E4M3) {
+        if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || !std::isfinite(c->k_scale) ||
+            !std::isfinite(c->v_scale))
+            return fail(PA_ERR_INVALID_ARG, "FP8 pools need finite positive k_scale and v_scale");
+        if (need_act && c->act_dtype != PA_BF16 && c->act_dtype != PA_F16)
+            return fail(PA_ERR_INVALID_ARG, "FP8 pools need act_dtype PA_BF16 or PA_F16");
+    }
     if (c->num_blocks <= 0 || c->n_kv_heads <= 0)
         return fail(PA_ERR_INVALID_ARG, "num_blocks and n_kv_heads must be positive");
     if (c->block_size != 16 && c->block_size != 32)
@@ -194,6 +205,34 @@ pa_status pa_get_device_error(void* stream)
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
     }
     return static_cast<pa_status>(v);
+}
+
+pa_status pa_reshape_and_cache_quant(const void* k, const void* v, pa_dtype in_dtype,
+                                     void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                                     int num_tokens, const pa_cache_desc* cache, void* stream)
+{
+    pa_status st = check_cache(cache, false);
+    if (st != PA_OK) return st;
+    if (in_dtype == cache->dtype)
+        return pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, num_tokens, cache, stream);
+    if (cache->dtype != PA_FP8_E4M3 ||
+        (in_dtype != PA_F32 && in_dtype != PA_F16 && in_dtype != PA_BF16))
+        return fail(PA_ERR_UNSUPPORTED, "cache write from dtype %d into dtype %d", (int)in_dtype,
+                    (int)cache->dtype);
+    if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (num_tokens == 0) return ok();
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "NULL pointer argument");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "k, v and the pools must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+        return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+    unsigned* err = device_error_word();
+    if (!err) return fail(PA_ERR_CUDA, "cannot locate the device error word");
+    cudaError_t e = launch_cache_write_fp8(k, v, in_dtype, k_cache, v_cache, slot_mapping,
+                                           num_tokens, *cache, err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cache write launch");
+    return ok();
 }
 
 pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
@@ -341,7 +380,7 @@ pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const v
     if (st != PA_OK) return st;
     if (num_reqs < 0 || max_query_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
     if (num_reqs == 0 || max_query_len == 0) return ok();
-    if (cache->dtype == PA_F32)
+    if (cache->dtype == PA_F32 || cache->dtype == PA_FP8_E4M3)
         return fail(PA_ERR_UNSUPPORTED, "chunked prefill runs on bf16/fp16 pools only");
     if (cache->head_dim != 64 && cache->head_dim != 128)
         return fail(PA_ERR_UNSUPPORTED, "chunked prefill supports head_dim 64 and 128");

@@ -26,12 +26,15 @@
 //     are handled as several 8-head sub-groups.
 // CUDA-core path (fp32, or shapes the tensor path does not cover): one warp
 // per query head, plain loads, fp32 FMA.
+#include <cuda_fp8.h>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 namespace pa {
 
@@ -50,28 +53,52 @@ __device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dt
         static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
-template <typename T, int D, int NS>
+// FP8 pools: a stage holds 16 rows of E4M3 codes of K and of V (no swizzle);
+// each warp widens them into one fp16 buffer laid out like a 16-bit stage.
+template <typename T, int D, int NS, bool FP8 = false>
 struct DecodeCfg {
-    static constexpr int kSlabBytes = kRows * D * static_cast<int>(sizeof(T));  // 16 rows of K or V
+    static constexpr int kElem = FP8 ? 1 : static_cast<int>(sizeof(T));
+    static constexpr int kSlabBytes = kRows * D * kElem;    // 16 rows of K or V as stored
     static constexpr int kStageBytes = 2 * kSlabBytes;
-    static constexpr int kWarpBytes = NS * kStageBytes;
+    static constexpr int kConvBytes = FP8 ? 2 * kRows * D * 2 : 0;   // widened K and V
+    static constexpr int kWarpBytes = NS * kStageBytes + kConvBytes;
     static constexpr int kRingBytes = kDecWarps * kWarpBytes;
     static constexpr int kReduceBytes = kDecWarps * 8 * (D + 2) * 4;
     static constexpr int kDynBytes = (kRingBytes > kReduceBytes ? kRingBytes : kReduceBytes) + 1024;
     static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
 };
 
-template <typename T, int D, int BS, int NS>
+// E4M3 pair -> fp16 pair (exact: every E4M3 value is an fp16 value)
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+template <typename QT, typename T>
+__device__ __forceinline__ uint32_t q_pair(const QT* p)
+{
+    return __ldg(reinterpret_cast<const unsigned int*>(p));   // q already in the MMA type
+}
+template <>
+__device__ __forceinline__ uint32_t q_pair<__nv_bfloat16, __half>(const __nv_bfloat16* p)
+{
+    const float2 f = Cvt<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const unsigned int*>(p)));
+    return Cvt<__half>::pack(f.x, f.y);
+}
+
+template <typename T, typename QT, int D, int BS, int NS, bool FP8>
 __global__ void __launch_bounds__(kDecWarps * 32, 2)
 decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  void* __restrict__ out, pa_dtype out_dtype, const T* __restrict__ q,
+                  void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
                   const int32_t* __restrict__ context_lens, int num_seqs, int n_q, int n_kv,
-                  int group, int num_blocks, float scale_log2, float* __restrict__ ws_ml,
-                  float* __restrict__ ws_acc, int part_tokens, int max_parts,
-                  unsigned* __restrict__ ticket, unsigned* err)
+                  int group, int num_blocks, float scale_log2, float v_scale,
+                  float* __restrict__ ws_ml, float* __restrict__ ws_acc, int part_tokens,
+                  int max_parts, unsigned* __restrict__ ticket, unsigned* err)
 {
-    using Cfg = DecodeCfg<T, D, NS>;
+    using Cfg = DecodeCfg<T, D, NS, FP8>;
+    static_assert(!FP8 || std::is_same<T, __half>::value, "FP8 pools compute in fp16");
     constexpr int kHalves = D / 64;           // 64-column halves (one 128-byte swizzled row each)
     constexpr int kHalfTile = kRows * 128;
     constexpr int kCPB = BS / kRows;          // stages per block
@@ -208,10 +235,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const uint32_t bar = bar0 + st * 8;
             const int row = (b * n_kv + kvh) * BS + (c % kCPB) * kRows;
             mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+            if constexpr (FP8) {
+                tma_load_2d(kdst, &kmap, 0, row, bar);   // 16 rows x D codes, unswizzled
+                tma_load_2d(vdst, &vmap, 0, row, bar);
+            } else {
 #pragma unroll
-            for (int hx = 0; hx < kHalves; ++hx) {
-                tma_load_2d(kdst + hx * kHalfTile, &kmap, hx * 64, row, bar);
-                tma_load_2d(vdst + hx * kHalfTile, &vmap, hx * 64, row, bar);
+                for (int hx = 0; hx < kHalves; ++hx) {
+                    tma_load_2d(kdst + hx * kHalfTile, &kmap, hx * 64, row, bar);
+                    tma_load_2d(vdst + hx * kHalfTile, &vmap, hx * 64, row, bar);
+                }
             }
         };
         if (lane == 0) {
@@ -224,9 +256,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             if (g < nh) {
-                const T* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
-                qa[kk][0] = __ldg(reinterpret_cast<const unsigned int*>(qp));
-                qa[kk][1] = __ldg(reinterpret_cast<const unsigned int*>(qp + 8));
+                const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
+                qa[kk][0] = q_pair<QT, T>(qp);
+                qa[kk][1] = q_pair<QT, T>(qp + 8);
             } else {
                 qa[kk][0] = 0u;
                 qa[kk][1] = 0u;
@@ -248,8 +280,40 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             const int pos0 = tok0 + (warp + k * kDecWarps) * kRows;
             const int valid = min(kRows, L - pos0);
-            const uint32_t kbase = ring + st * Cfg::kStageBytes;
-            const uint32_t vbase = kbase + Cfg::kSlabBytes;
+            uint32_t kbase = ring + st * Cfg::kStageBytes;
+            uint32_t vbase = kbase + Cfg::kSlabBytes;
+            if constexpr (FP8) {
+                // widen the stage's codes into the warp's fp16 buffer (the
+                // 128-byte swizzled layout the ldmatrix addressing below expects),
+                // then hand the stage straight back to the TMA ring
+                const uint32_t conv = ring + NS * Cfg::kStageBytes;
+                const uint8_t* src = smem + (kbase - smem_u32(smem));
+                uint8_t* dstg = smem + (conv - smem_u32(smem));
+                constexpr int kPieces = kRows * D / 16;        // 16-byte pieces per matrix
+#pragma unroll
+                for (int mtx = 0; mtx < 2; ++mtx) {
+                    for (int pc = lane; pc < kPieces; pc += 32) {
+                        const uint4 c8 = *reinterpret_cast<const uint4*>(src + mtx * Cfg::kSlabBytes + pc * 16);
+                        const int r = pc / (D / 16);
+                        const int col = (pc - r * (D / 16)) * 16;          // first element
+                        const int ch = col >> 3;                             // 16-byte fp16 chunk
+                        uint8_t* rowp = dstg + mtx * (kRows * D * 2) + (ch >> 3) * kHalfTile + r * 128;
+                        const uint4 lo = make_uint4(e4m3x2_to_h2(c8.x & 0xFFFF), e4m3x2_to_h2(c8.x >> 16),
+                                                    e4m3x2_to_h2(c8.y & 0xFFFF), e4m3x2_to_h2(c8.y >> 16));
+                        const uint4 hi = make_uint4(e4m3x2_to_h2(c8.z & 0xFFFF), e4m3x2_to_h2(c8.z >> 16),
+                                                    e4m3x2_to_h2(c8.w & 0xFFFF), e4m3x2_to_h2(c8.w >> 16));
+                        *reinterpret_cast<uint4*>(rowp + (((ch & 7) ^ (r & 7)) << 4)) = lo;
+                        *reinterpret_cast<uint4*>(rowp + ((((ch + 1) & 7) ^ (r & 7)) << 4)) = hi;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0 && k + NS < my_n) {
+                    fence_proxy_async_smem();
+                    issue(k + NS);
+                }
+                kbase = conv;
+                vbase = conv + kRows * D * 2;
+            }
 
             if (valid < kRows) {
                 // rows past the sequence may hold anything (even NaN): zero them in
@@ -333,7 +397,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
 
             __syncwarp();
-            if (lane == 0 && k + NS < my_n) {
+            if (!FP8 && lane == 0 && k + NS < my_n) {
                 fence_proxy_async_smem();
                 issue(k + NS);
             }
@@ -371,6 +435,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 lsum += f * red_l[w * 8 + hh];
                 acc += f * red_o[(w * 8 + hh) * D + dd];
             }
+            acc *= v_scale;                                    // 1 unless the pool is FP8
             const int64_t sh = static_cast<int64_t>(s) * n_q + h0 + hh;
             if (nparts == 1) {
                 store_any(out, sh * D + dd, acc / lsum, out_dtype);
@@ -519,14 +584,16 @@ static int sm_count()
     return cache[dev];
 }
 
-template <typename T, int D, int BS>
+template <typename T, typename QT, int D, int BS, bool FP8>
 static cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
 {
-    // ring depth per warp: about 24 KB of K+V in flight per warp, at least 2 stages
-    constexpr int kStage = 2 * kRows * D * static_cast<int>(sizeof(T));
-    constexpr int NS = 24576 / kStage > 2 ? 24576 / kStage : 2;
-    using Cfg = DecodeCfg<T, D, NS>;
-    auto kern = decode_mma_kernel<T, D, BS, NS>;
+    // ring depth per warp: about 24 KB of K+V in flight per warp (16 KB for FP8,
+    // which also keeps an 8 KB widened buffer), at least 2 stages
+    constexpr int kStage = 2 * kRows * D * (FP8 ? 1 : static_cast<int>(sizeof(T)));
+    constexpr int kBudget = FP8 ? 16384 : 24576;
+    constexpr int NS = kBudget / kStage > 2 ? kBudget / kStage : 2;
+    using Cfg = DecodeCfg<T, D, NS, FP8>;
+    auto kern = decode_mma_kernel<T, QT, D, BS, NS, FP8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int per_sm = 1;
@@ -542,8 +609,9 @@ static cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap kmap, vmap;
     const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
-    if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK ||
-        encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK)
+    const int box_x = FP8 ? D : 64;
+    if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, box_x, kRows, !FP8) != PA_OK ||
+        encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, box_x, kRows, !FP8) != PA_OK)
         return cudaErrorInvalidValue;
     const int group = a.n_q / a.cache.n_kv_heads;
     const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.max_parts * a.cache.n_kv_heads *
@@ -551,9 +619,10 @@ static cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2
     const int64_t resident = static_cast<int64_t>(sm_count()) * per_sm;
     const unsigned grid = static_cast<unsigned>(upper < resident ? upper : resident);
     kern<<<grid, kDecWarps * 32, Cfg::kDynBytes, s>>>(
-        kmap, vmap, a.out, a.out_dtype, static_cast<const T*>(a.q), a.block_tables, a.max_blocks,
+        kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
         a.context_lens, a.num_seqs, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
-        scale_log2, a.ws_ml, a.ws_acc, a.part_tokens, a.max_parts, a.ticket, a.err);
+        FP8 ? scale_log2 * a.cache.k_scale : scale_log2, FP8 ? a.cache.v_scale : 1.f, a.ws_ml,
+        a.ws_acc, a.part_tokens, a.max_parts, a.ticket, a.err);
     return cudaGetLastError();
 }
 
@@ -586,11 +655,22 @@ template <typename T>
 static cudaError_t run_mma_dt(const DecodeArgs& a, cudaStream_t s, float sl2)
 {
     const int D = a.cache.head_dim, BS = a.cache.block_size;
-    if (D == 64 && BS == 16) return run_mma<T, 64, 16>(a, s, sl2);
-    if (D == 64 && BS == 32) return run_mma<T, 64, 32>(a, s, sl2);
-    if (D == 128 && BS == 16) return run_mma<T, 128, 16>(a, s, sl2);
-    if (D == 128 && BS == 32) return run_mma<T, 128, 32>(a, s, sl2);
+    if (D == 64 && BS == 16) return run_mma<T, T, 64, 16, false>(a, s, sl2);
+    if (D == 64 && BS == 32) return run_mma<T, T, 64, 32, false>(a, s, sl2);
+    if (D == 128 && BS == 16) return run_mma<T, T, 128, 16, false>(a, s, sl2);
+    if (D == 128 && BS == 32) return run_mma<T, T, 128, 32, false>(a, s, sl2);
     return run_simt_dt<T>(a, s, sl2);
+}
+
+template <typename QT>
+static cudaError_t run_fp8_qt(const DecodeArgs& a, cudaStream_t s, float sl2)
+{
+    const int D = a.cache.head_dim, BS = a.cache.block_size;
+    if (D == 64 && BS == 16) return run_mma<__half, QT, 64, 16, true>(a, s, sl2);
+    if (D == 64 && BS == 32) return run_mma<__half, QT, 64, 32, true>(a, s, sl2);
+    if (D == 128 && BS == 16) return run_mma<__half, QT, 128, 16, true>(a, s, sl2);
+    if (D == 128 && BS == 32) return run_mma<__half, QT, 128, 32, true>(a, s, sl2);
+    return cudaErrorInvalidValue;
 }
 
 static cudaError_t run_reduce(const DecodeArgs& a, cudaStream_t s)
@@ -616,7 +696,7 @@ static cudaError_t run_reduce(const DecodeArgs& a, cudaStream_t s)
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
 {
     const float sl2 = a.scale * 1.4426950408889634f;   // softmax in base 2
-    if (a.cache.dtype != PA_F32) {
+    if (a.cache.dtype != PA_F32) {   // the tensor-core kernels take work from a counter
         cudaError_t e0 = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), s);
         if (e0 != cudaSuccess) return e0;
     }
@@ -627,6 +707,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     switch (a.cache.dtype) {
         case PA_BF16: e = run_mma_dt<__nv_bfloat16>(a, s, sl2); break;
         case PA_F16: e = run_mma_dt<__half>(a, s, sl2); break;
+        case PA_FP8_E4M3:
+            e = a.cache.act_dtype == PA_BF16 ? run_fp8_qt<__nv_bfloat16>(a, s, sl2)
+                                             : run_fp8_qt<__half>(a, s, sl2);
+            break;
         default: e = run_simt_dt<float>(a, s, sl2); break;
     }
     if (ev1) cudaEventRecord(ev1, s);

@@ -23,17 +23,20 @@ unsigned* device_error_word();
 // Encodes a 2-D tiled tensor map over a pool viewed as rows of head_dim
 // elements: dims {head_dim, rows}, box {box_x, box_y}, 128-byte swizzle.
 pa_status encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int head_dim,
-                          uint64_t rows, int box_x, int box_y);
+                          uint64_t rows, int box_x, int box_y, bool swizzle128 = true);
 
 // Profiling events for the main decode kernel (may be null).
 void profile_events(cudaEvent_t* start, cudaEvent_t* stop);
 
-inline int elem_bytes(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
+inline int elem_bytes(pa_dtype d) { return d == PA_F32 ? 4 : (d == PA_FP8_E4M3 ? 1 : 2); }
 
 // ---- launchers (defined next to their kernels) ----
 cudaError_t launch_cache_write(const void* k, const void* v, void* kc, void* vc,
                                const int64_t* slots, int T, const pa_cache_desc& c,
                                unsigned* err, cudaStream_t s);
+cudaError_t launch_cache_write_fp8(const void* k, const void* v, pa_dtype in_dtype, void* kc,
+                                   void* vc, const int64_t* slots, int T, const pa_cache_desc& c,
+                                   unsigned* err, cudaStream_t s);
 
 cudaError_t launch_copy_blocks(const void* src_k, const void* src_v, int src_blocks, void* dst_k,
                                void* dst_v, int dst_blocks, const pa_cache_desc& layout,

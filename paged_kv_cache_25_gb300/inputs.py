@@ -21,6 +21,8 @@ Workloads (the KV shapes are single transformer layers):
                      bs 16, bf16, pool 1.5x the blocks needed.
 * ``opt13b-fp16``    128 sequences, every length 2048, 40/40 heads, d 128, bs 16,
                      fp16, values N(0, 0.5) (standard deviation 0.5).
+* ``llama3-8b-fp8``  the Llama-3-8B decode batch (same draws) stored in an FP8
+                     E4M3 pool with K and V scale 1/64.
 * ``mixed-llama3-8b-bf16``  one continuous-batching step on Llama-3-8B shapes with
                      bs 32: 192 decode sequences with lengths lognormal(7, 1)
                      clipped to [16, 32768], a quarter of them sharing one
@@ -67,6 +69,16 @@ class Workload:
     prefill_requests: int = 0
     prefill_chunk: int = 0
     prefill_ctx_range: tuple = (0, 0)
+    cache_dtype: torch.dtype | None = None   # pool dtype when it differs (FP8 pools)
+    kv_scale: float = 1.0                     # FP8 pools: per-tensor scale of K and V
+
+    @property
+    def pool_dtype(self) -> torch.dtype:
+        return self.cache_dtype or self.dtype
+
+    @property
+    def pool_elem_bytes(self) -> int:
+        return torch.empty((), dtype=self.pool_dtype).element_size()
 
     @property
     def group(self) -> int:
@@ -92,6 +104,10 @@ WORKLOADS = {
                                lens_kind="uniform", lens_args=(512, 4096)),
     "opt13b-fp16": Workload("opt13b-fp16", 1004, 128, 40, 40, 128, 16, torch.float16, std=0.5,
                             lens_kind="const", lens_args=(2048,)),
+    # the Llama-3-8B decode batch with an FP8 E4M3 pool (K and V scale 1/64)
+    "llama3-8b-fp8": Workload("llama3-8b-fp8", 1003, 256, 32, 8, 128, 16, torch.bfloat16,
+                              lens_kind="uniform", lens_args=(512, 4096),
+                              cache_dtype=torch.float8_e4m3fn, kv_scale=1.0 / 64),
     "mixed-llama3-8b-bf16": Workload("mixed-llama3-8b-bf16", 1005, 192, 32, 8, 128, 32,
                                      torch.bfloat16, lens_kind="lognormal",
                                      lens_args=(7.0, 1.0, 16, 32768),
@@ -224,7 +240,8 @@ class Draws:
 
 
 def random_case(seed: int, batch: int, n_q: int, n_kv: int, d: int, bs: int, dtype, lens,
-                std: float = 1.0) -> Workload:
+                std: float = 1.0, cache_dtype=None, kv_scale: float = 1.0) -> Workload:
     """An ad-hoc workload for property tests (explicit lengths, 1.5x pool)."""
     return Workload(f"case-{seed}", seed, batch, n_q, n_kv, d, bs, dtype, std=std,
-                    lens_kind="list", lens_args=tuple(int(x) for x in lens))
+                    lens_kind="list", lens_args=tuple(int(x) for x in lens),
+                    cache_dtype=cache_dtype, kv_scale=kv_scale)

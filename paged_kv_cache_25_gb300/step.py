@@ -43,7 +43,9 @@ class PagedStep:
         self.R = len(self.p_lens)
 
         # ---- pool size and block tables (library allocator) ----------------
-        per_tok = pa.pa_kv_bytes_per_token(1, n_kv, d, wl.elem_bytes)
+        per_tok = pa.pa_kv_bytes_per_token(1, n_kv, d, wl.pool_elem_bytes)
+        self.fp8 = wl.pool_dtype == torch.float8_e4m3fn
+        self.kv_scales = dict(k_scale=wl.kv_scale, v_scale=wl.kv_scale) if self.fp8 else {}
         need = int(sum(_ceil_div(int(L), bs) for L in self.lens))
         if self.prefix:
             need -= (int(self.sharers.sum()) - 1) * (self.prefix // bs)
@@ -64,8 +66,14 @@ class PagedStep:
                          if self.R else np.zeros((0, self.max_blocks), np.int32))
 
         dev = self.device
-        self.k_cache = torch.full((nb, n_kv, bs, d), float("nan"), dtype=wl.dtype, device=dev)
-        self.v_cache = torch.full((nb, n_kv, bs, d), float("nan"), dtype=wl.dtype, device=dev)
+        # unwritten slots hold NaN (E4M3 NaN code 0x7F for FP8 pools)
+        if self.fp8:
+            self.k_cache = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8,
+                                      device=dev).view(torch.float8_e4m3fn)
+            self.v_cache = self.k_cache.clone()
+        else:
+            self.k_cache = torch.full((nb, n_kv, bs, d), float("nan"), dtype=wl.dtype, device=dev)
+            self.v_cache = torch.full((nb, n_kv, bs, d), float("nan"), dtype=wl.dtype, device=dev)
 
         # ---- pre-fill the cached context through the cache-write kernel ------
         self._prefill_context(upload_chunk_tokens)
@@ -125,7 +133,7 @@ class PagedStep:
             k = torch.cat(pending_k).to(self.device, non_blocking=False).contiguous()
             v = torch.cat(pending_v).to(self.device, non_blocking=False).contiguous()
             s = torch.from_numpy(np.concatenate(pending_s)).to(self.device)
-            pa.pa_reshape_and_cache(k, v, self.k_cache, self.v_cache, s)
+            self._write(k, v, s)
             torch.cuda.synchronize(self.device)
             pending_k, pending_v, pending_s, n = [], [], [], 0
 
@@ -154,16 +162,23 @@ class PagedStep:
             add(k, v, self.p_tables, r, 0, int(self.p_ctx[r]))
         flush()
 
+    def _write(self, k, v, slots, stream=None):
+        if self.fp8:
+            pa.pa_reshape_and_cache_quant(k, v, self.k_cache, self.v_cache, slots, stream=stream,
+                                          **self.kv_scales)
+        else:
+            pa.pa_reshape_and_cache(k, v, self.k_cache, self.v_cache, slots, stream=stream)
+
     # ------------------------------------------------------------------
     def step(self, stream=None, prefill_events=None):
         """One pass of the hot path; all work is enqueued on `stream`.
         prefill_events: optional (start, stop) torch.cuda.Event pair recorded
         around the chunked-prefill kernel."""
         wl = self.wl
-        pa.pa_reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache,
-                                self.new_slots, stream=stream)
+        self._write(self.new_k, self.new_v, self.new_slots, stream=stream)
         pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
-                     self.context_lens, wl.scale, wl.block_size, self.workspace, stream=stream)
+                     self.context_lens, wl.scale, wl.block_size, self.workspace, stream=stream,
+                     **self.kv_scales)
         if self.R:
             if prefill_events is not None:
                 prefill_events[0].record(stream or torch.cuda.current_stream())
@@ -177,7 +192,7 @@ class PagedStep:
     def kv_bytes_unique(self) -> int:
         """K+V bytes the decode must read: valid rows of distinct physical blocks."""
         wl, bs = self.wl, self.wl.block_size
-        row = 2 * wl.n_kv_heads * wl.head_dim * wl.elem_bytes
+        row = 2 * wl.n_kv_heads * wl.head_dim * wl.pool_elem_bytes
         seen = {}
         for s, L in enumerate(self.lens):
             for i in range(_ceil_div(int(L), bs)):
@@ -187,7 +202,7 @@ class PagedStep:
 
     def kv_bytes_logical(self) -> int:
         wl = self.wl
-        return int(self.lens.sum()) * 2 * wl.n_kv_heads * wl.head_dim * wl.elem_bytes
+        return int(self.lens.sum()) * 2 * wl.n_kv_heads * wl.head_dim * wl.pool_elem_bytes
 
     def prefill_flops(self) -> int:
         """2 matmuls x 2 flops per MAC over the causal (query, key) pairs."""

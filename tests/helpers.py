@@ -21,6 +21,16 @@ def half_ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
     return 0.5 * np.exp2(e - (mant - 1))
 
 
+def stored_kv(wl, k, v):
+    """The K/V values a pool of the workload holds for rows k, v: the rows
+    themselves, or for FP8 pools the oracle's E4M3 codes times the scale."""
+    if wl.pool_dtype != torch.float8_e4m3fn:
+        return k, v
+    kq = oracle.dequantize_fp8(oracle.quantize_fp8(k, wl.kv_scale), wl.kv_scale)
+    vq = oracle.dequantize_fp8(oracle.quantize_fp8(v, wl.kv_scale), wl.kv_scale)
+    return kq, vq
+
+
 def oracle_decode(step, seqs=None, threads=None) -> np.ndarray:
     """fp64 decode for the given decode sequences of a PagedStep's workload."""
     dr, wl = step.draws, step.wl
@@ -29,6 +39,7 @@ def oracle_decode(step, seqs=None, threads=None) -> np.ndarray:
     ks, vs = [], []
     for s in seqs:
         k, v = dr.seq_kv(s, int(step.lens[s]), bool(step.sharers[s]), prefix)
+        k, v = stored_kv(wl, k, v)
         ks.append(k); vs.append(v)
     q = dr.q()[seqs]
     return oracle.decode(q, ks, vs, wl.scale, threads=threads)
