@@ -67,7 +67,10 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
  * 1 byte per element if the cache is quantized to FP8): dtype PA_FP8_E4M3,
  * each stored code c means decode_e4m3(c) * k_scale for K (v_scale for V);
  * act_dtype (PA_BF16 or PA_F16) is the dtype of q and of the K/V rows given
- * to pa_reshape_and_cache_quant.  The three fields are ignored otherwise. */
+ * to pa_reshape_and_cache_quant.  The three fields are ignored otherwise.
+ * In FP8 pools the V codes of each (block, KV head) are stored transposed,
+ * v_cache [num_blocks][n_kv_heads][head_dim][block_size], so that the decode
+ * kernel reads pairs of tokens per head-dim element; K keeps the layout above. */
 typedef struct {
     int num_blocks;
     int block_size;

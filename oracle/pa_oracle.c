@@ -158,6 +158,24 @@ void orc_cache_write(uint8_t* k_cache, uint8_t* v_cache, const uint8_t* k, const
     }
 }
 
+void orc_cache_write_vt(uint8_t* v_cache, const uint8_t* v, const int64_t* slots, int T,
+                        int num_blocks, int n_kv, int block_size, int head_dim, int elem_bytes)
+{
+    for (int t = 0; t < T; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0) continue;
+        int64_t b = slot / block_size, o = slot % block_size;
+        if (b >= num_blocks) continue;
+        for (int h = 0; h < n_kv; ++h)
+            for (int i = 0; i < head_dim; ++i) {
+                size_t dst = ((((size_t)b * n_kv + h) * head_dim + (size_t)i) * block_size + (size_t)o) *
+                             elem_bytes;
+                size_t src = (((size_t)t * n_kv + h) * head_dim + (size_t)i) * elem_bytes;
+                memcpy(v_cache + dst, v + src, (size_t)elem_bytes);
+            }
+    }
+}
+
 void orc_copy_blocks(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k, uint8_t* dst_v,
                      const int32_t* map, int n, int64_t block_bytes)
 {

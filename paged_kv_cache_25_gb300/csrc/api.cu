@@ -72,7 +72,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 pa_status encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int head_dim,
-                          uint64_t rows, int box_x, int box_y, bool swizzle128)
+                          uint64_t rows, int box_x, int box_y, int swizzle)
 {
     auto fn = encode_fn();
     if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -85,7 +85,9 @@ pa_status encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int h
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, t, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                         : (swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                          : CU_TENSOR_MAP_SWIZZLE_NONE),
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return PA_OK;
@@ -330,6 +332,8 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_
     if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
     if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (1 << 30))
         return fail(PA_ERR_UNSUPPORTED, "max context above 2^30 tokens");
+    if (cache->dtype == PA_FP8_E4M3 && cache->head_dim != 64 && cache->head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "FP8 pools decode with head_dim 64 or 128");
 
     const int max_ctx = max_blocks_per_seq * block_size;
     int part = 0, parts = 0;

@@ -55,8 +55,9 @@ cudaError_t launch_cache_write(const void* k, const void* v, void* kc, void* vc,
 }
 
 // Quantizing write into an FP8 E4M3 pool: one thread turns 16 input elements
-// of one (token, head) row into 16 codes (one 16-byte store): code =
-// e4m3_rn_satfinite(x / scale) with x / scale an IEEE fp32 division.
+// of one (token, head) row into 16 codes: code = e4m3_rn_satfinite(x / scale)
+// with x / scale an IEEE fp32 division.  K codes are one 16-byte store; V
+// codes go to the transposed V slab, one column of [head_dim][block_size].
 template <typename TI>
 __device__ __forceinline__ float load_as_float(const TI* p, int i);
 template <> __device__ __forceinline__ float load_as_float<float>(const float* p, int i) { return p[i]; }
@@ -109,7 +110,13 @@ cache_write_fp8_kernel(const TI* __restrict__ k, const TI* __restrict__ v, uint4
     const int64_t dst = ((b * n_kv + h) * block_size + o) * pieces_per_row + c;
     const int64_t src = i * 16;                   // element offset of this piece
     kc[dst] = quant16(k + src, k_scale);
-    vc[dst] = quant16(v + src, v_scale);
+    // V codes are stored transposed per (block, head): [head_dim][block_size]
+    const uint4 vq = quant16(v + src, v_scale);
+    uint8_t* vcol = reinterpret_cast<uint8_t*>(vc) +
+                    ((b * n_kv + h) * (pieces_per_row * 16) + c * 16) * block_size + o;
+    const uint32_t w[4] = {vq.x, vq.y, vq.z, vq.w};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) vcol[e * block_size] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
 }
 
 cudaError_t launch_cache_write_fp8(const void* k, const void* v, pa_dtype in_dtype, void* kc,

@@ -53,15 +53,14 @@ __device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dt
         static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
-// FP8 pools: a stage holds 16 rows of E4M3 codes of K and of V (no swizzle);
-// each warp widens them into one fp16 buffer laid out like a 16-bit stage.
+// FP8 pools: a stage holds 16 rows of E4M3 K codes (swizzled rows of D bytes)
+// and the matching D x 16 tile of the transposed V codes.
 template <typename T, int D, int NS, bool FP8 = false>
 struct DecodeCfg {
     static constexpr int kElem = FP8 ? 1 : static_cast<int>(sizeof(T));
     static constexpr int kSlabBytes = kRows * D * kElem;    // 16 rows of K or V as stored
     static constexpr int kStageBytes = 2 * kSlabBytes;
-    static constexpr int kConvBytes = FP8 ? 2 * kRows * D * 2 : 0;   // widened K and V
-    static constexpr int kWarpBytes = NS * kStageBytes + kConvBytes;
+    static constexpr int kWarpBytes = NS * kStageBytes;
     static constexpr int kRingBytes = kDecWarps * kWarpBytes;
     static constexpr int kReduceBytes = kDecWarps * 8 * (D + 2) * 4;
     static constexpr int kDynBytes = (kRingBytes > kReduceBytes ? kRingBytes : kReduceBytes) + 1024;
@@ -236,8 +235,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const int row = (b * n_kv + kvh) * BS + (c % kCPB) * kRows;
             mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
             if constexpr (FP8) {
-                tma_load_2d(kdst, &kmap, 0, row, bar);   // 16 rows x D codes, unswizzled
-                tma_load_2d(vdst, &vmap, 0, row, bar);
+                tma_load_2d(kdst, &kmap, 0, row, bar);                       // 16 rows x D codes
+                tma_load_2d(vdst, &vmap, (c % kCPB) * kRows, (b * n_kv + kvh) * D, bar);  // D x 16
             } else {
 #pragma unroll
                 for (int hx = 0; hx < kHalves; ++hx) {
@@ -256,9 +255,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             if (g < nh) {
-                const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
-                qa[kk][0] = q_pair<QT, T>(qp);
-                qa[kk][1] = q_pair<QT, T>(qp + 8);
+                if constexpr (FP8) {
+                    // k order of the FP8 fragments: columns 4*t4 .. 4*t4+3 of the chunk
+                    const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 4 * t4;
+                    qa[kk][0] = q_pair<QT, T>(qp);
+                    qa[kk][1] = q_pair<QT, T>(qp + 2);
+                } else {
+                    const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
+                    qa[kk][0] = q_pair<QT, T>(qp);
+                    qa[kk][1] = q_pair<QT, T>(qp + 8);
+                }
             } else {
                 qa[kk][0] = 0u;
                 qa[kk][1] = 0u;
@@ -280,71 +286,79 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             const int pos0 = tok0 + (warp + k * kDecWarps) * kRows;
             const int valid = min(kRows, L - pos0);
-            uint32_t kbase = ring + st * Cfg::kStageBytes;
-            uint32_t vbase = kbase + Cfg::kSlabBytes;
+            const uint32_t kbase = ring + st * Cfg::kStageBytes;
+            const uint32_t vbase = kbase + Cfg::kSlabBytes;
+            float sc[2][4];
+
             if constexpr (FP8) {
-                // widen the stage's codes into the warp's fp16 buffer (the
-                // 128-byte swizzled layout the ldmatrix addressing below expects),
-                // then hand the stage straight back to the TMA ring
-                const uint32_t conv = ring + NS * Cfg::kStageBytes;
-                const uint8_t* src = smem + (kbase - smem_u32(smem));
-                uint8_t* dstg = smem + (conv - smem_u32(smem));
-                constexpr int kPieces = kRows * D / 16;        // 16-byte pieces per matrix
+                if (valid < kRows) {
+                    // tokens past the sequence may hold anything (even NaN): zero
+                    // their codes in every row of the transposed V tile
+                    uint8_t* vt = smem + (vbase - smem_u32(smem));
+                    for (int row = lane; row < D; row += 32) {
+                        uint4 w = *reinterpret_cast<uint4*>(vt + row * 16);
+                        uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-                for (int mtx = 0; mtx < 2; ++mtx) {
-                    for (int pc = lane; pc < kPieces; pc += 32) {
-                        const uint4 c8 = *reinterpret_cast<const uint4*>(src + mtx * Cfg::kSlabBytes + pc * 16);
-                        const int r = pc / (D / 16);
-                        const int col = (pc - r * (D / 16)) * 16;          // first element
-                        const int ch = col >> 3;                             // 16-byte fp16 chunk
-                        uint8_t* rowp = dstg + mtx * (kRows * D * 2) + (ch >> 3) * kHalfTile + r * 128;
-                        const uint4 lo = make_uint4(e4m3x2_to_h2(c8.x & 0xFFFF), e4m3x2_to_h2(c8.x >> 16),
-                                                    e4m3x2_to_h2(c8.y & 0xFFFF), e4m3x2_to_h2(c8.y >> 16));
-                        const uint4 hi = make_uint4(e4m3x2_to_h2(c8.z & 0xFFFF), e4m3x2_to_h2(c8.z >> 16),
-                                                    e4m3x2_to_h2(c8.w & 0xFFFF), e4m3x2_to_h2(c8.w >> 16));
-                        *reinterpret_cast<uint4*>(rowp + (((ch & 7) ^ (r & 7)) << 4)) = lo;
-                        *reinterpret_cast<uint4*>(rowp + ((((ch + 1) & 7) ^ (r & 7)) << 4)) = hi;
+                        for (int e = 0; e < 4; ++e) {
+                            const int keep = min(4, max(0, valid - 4 * e));     // bytes kept
+                            ww[e] &= keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+                        }
+                        *reinterpret_cast<uint4*>(vt + row * 16) = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                // S = Q K^T.  Column j of n-tile nt is token 4*(j/2) + 2*nt + j%2,
+                // which leaves P in the token order the V fragments use below.
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                    const int i = lane & 7;
+                    const int r = 4 * (i >> 1) + 2 * nt + (i & 1);
+#pragma unroll
+                    for (int kq = 0; kq < D / 64; ++kq) {
+                        const int cidx = kq * 4 + (lane >> 3);
+                        const int sw = D == 128 ? (cidx ^ (r & 7)) : (cidx ^ ((r >> 1) & 3));
+                        uint32_t w[4];
+                        ldsm_x4(kbase + r * D + (sw << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int kk = kq * 4 + jj;
+                            const uint32_t a[4] = {qa[kk][0], 0u, qa[kk][1], 0u};
+                            MmaOp<T>::run(sc[nt], a, e4m3x2_to_h2(w[jj] & 0xFFFF), e4m3x2_to_h2(w[jj] >> 16));
+                        }
                     }
                 }
-                __syncwarp();
-                if (lane == 0 && k + NS < my_n) {
+            } else {
+                if (valid < kRows) {
+                    // rows past the sequence may hold anything (even NaN): zero them in
+                    // V so that 0 * row stays 0 inside the MMA
+                    uint8_t* vgen = smem + (vbase - smem_u32(smem));
+                    const int nbytes = (kRows - valid) * 128;
+                    for (int hx = 0; hx < kHalves; ++hx)
+                        for (int off = lane * 16; off < nbytes; off += 32 * 16)
+                            *reinterpret_cast<uint4*>(vgen + hx * kHalfTile + valid * 128 + off) =
+                                make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();
-                    issue(k + NS);
+                    __syncwarp();
                 }
-                kbase = conv;
-                vbase = conv + kRows * D * 2;
-            }
-
-            if (valid < kRows) {
-                // rows past the sequence may hold anything (even NaN): zero them in
-                // V so that 0 * row stays 0 inside the MMA
-                uint8_t* vgen = smem + (vbase - smem_u32(smem));
-                const int nbytes = (kRows - valid) * 128;
-                for (int hx = 0; hx < kHalves; ++hx)
-                    for (int off = lane * 16; off < nbytes; off += 32 * 16)
-                        *reinterpret_cast<uint4*>(vgen + hx * kHalfTile + valid * 128 + off) =
-                            make_uint4(0, 0, 0, 0);
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-
-            // S = Q K^T for the 16 rows
-            float sc[2][4];
+                // S = Q K^T for the 16 rows
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                for (int nt = 0; nt < 2; ++nt) {
+                    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-                for (int kc = 0; kc < D / 16; kc += 2) {
-                    const int r = nt * 8 + (lane & 7);
-                    const int chunk = kc * 2 + (lane >> 3);
-                    const uint32_t addr = kbase + (chunk >> 3) * kHalfTile + r * 128 +
-                                          (((chunk & 7) ^ (r & 7)) << 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(addr, b0, b1, b2, b3);
-                    const uint32_t a0[4] = {qa[kc][0], 0u, qa[kc][1], 0u};
-                    const uint32_t a1[4] = {qa[kc + 1][0], 0u, qa[kc + 1][1], 0u};
-                    MmaOp<T>::run(sc[nt], a0, b0, b1);
-                    MmaOp<T>::run(sc[nt], a1, b2, b3);
+                    for (int kc = 0; kc < D / 16; kc += 2) {
+                        const int r = nt * 8 + (lane & 7);
+                        const int chunk = kc * 2 + (lane >> 3);
+                        const uint32_t addr = kbase + (chunk >> 3) * kHalfTile + r * 128 +
+                                              (((chunk & 7) ^ (r & 7)) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(addr, b0, b1, b2, b3);
+                        const uint32_t a0[4] = {qa[kc][0], 0u, qa[kc][1], 0u};
+                        const uint32_t a1[4] = {qa[kc + 1][0], 0u, qa[kc + 1][1], 0u};
+                        MmaOp<T>::run(sc[nt], a0, b0, b1);
+                        MmaOp<T>::run(sc[nt], a1, b2, b3);
+                    }
                 }
             }
 
@@ -354,7 +368,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int p = pos0 + nt * 8 + 2 * t4 + e;
+                    const int p = pos0 + (FP8 ? 4 * t4 + 2 * nt + e : nt * 8 + 2 * t4 + e);
                     const float z = p < L ? sc[nt][e] * scale_log2 : -INFINITY;
                     sc[nt][e] = z;
                     mx = fmaxf(mx, z);
@@ -383,21 +397,35 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             uint32_t pa[4];
             split_pair<T>(sc[0][0], sc[0][1], pa[0], pa[1]);
             split_pair<T>(sc[1][0], sc[1][1], pa[2], pa[3]);
+            if constexpr (FP8) {
+                // transposed V tile: row d holds tokens 0..15; a fragment word is
+                // tokens 4*t4 .. 4*t4+3 of row d, the k order P is in
 #pragma unroll
-            for (int nt = 0; nt < D / 8; nt += 2) {
-                const int mi = lane >> 3;
-                const int r = (mi & 1) * 8 + (lane & 7);
-                const int chunk = nt + (mi >> 1);
-                const uint32_t addr = vbase + (chunk >> 3) * kHalfTile + r * 128 +
-                                      (((chunk & 7) ^ (r & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(addr, b0, b1, b2, b3);
-                MmaOp<T>::run(o[nt], pa, b0, b1);
-                MmaOp<T>::run(o[nt + 1], pa, b2, b3);
+                for (int nd = 0; nd < D / 8; nd += 4) {
+                    const int d_row = (nd + (lane >> 3)) * 8 + (lane & 7);
+                    uint32_t w[4];
+                    ldsm_x4(vbase + d_row * 16, w[0], w[1], w[2], w[3]);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        MmaOp<T>::run(o[nd + jj], pa, e4m3x2_to_h2(w[jj] & 0xFFFF), e4m3x2_to_h2(w[jj] >> 16));
+                }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < D / 8; nt += 2) {
+                    const int mi = lane >> 3;
+                    const int r = (mi & 1) * 8 + (lane & 7);
+                    const int chunk = nt + (mi >> 1);
+                    const uint32_t addr = vbase + (chunk >> 3) * kHalfTile + r * 128 +
+                                          (((chunk & 7) ^ (r & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(addr, b0, b1, b2, b3);
+                    MmaOp<T>::run(o[nt], pa, b0, b1);
+                    MmaOp<T>::run(o[nt + 1], pa, b2, b3);
+                }
             }
 
             __syncwarp();
-            if (!FP8 && lane == 0 && k + NS < my_n) {
+            if (lane == 0 && k + NS < my_n) {
                 fence_proxy_async_smem();
                 issue(k + NS);
             }
@@ -590,7 +618,7 @@ static cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2
     // ring depth per warp: about 24 KB of K+V in flight per warp (16 KB for FP8,
     // which also keeps an 8 KB widened buffer), at least 2 stages
     constexpr int kStage = 2 * kRows * D * (FP8 ? 1 : static_cast<int>(sizeof(T)));
-    constexpr int kBudget = FP8 ? 16384 : 24576;
+    constexpr int kBudget = 24576;
     constexpr int NS = kBudget / kStage > 2 ? kBudget / kStage : 2;
     using Cfg = DecodeCfg<T, D, NS, FP8>;
     auto kern = decode_mma_kernel<T, QT, D, BS, NS, FP8>;
@@ -609,10 +637,19 @@ static cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap kmap, vmap;
     const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
-    const int box_x = FP8 ? D : 64;
-    if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, box_x, kRows, !FP8) != PA_OK ||
-        encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, box_x, kRows, !FP8) != PA_OK)
-        return cudaErrorInvalidValue;
+    if constexpr (FP8) {
+        // K: rows of D codes, 128- (D 128) or 64-byte (D 64) swizzle; V: the
+        // transposed slabs viewed as rows of block_size codes, one row per
+        // (block, head, head-dim element)
+        const uint64_t vrows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * D;
+        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, D, kRows, D) != PA_OK ||
+            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, BS, vrows, kRows, D, 0) != PA_OK)
+            return cudaErrorInvalidValue;
+    } else {
+        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK ||
+            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK)
+            return cudaErrorInvalidValue;
+    }
     const int group = a.n_q / a.cache.n_kv_heads;
     const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.max_parts * a.cache.n_kv_heads *
                           ((group + 7) / 8);

@@ -22,8 +22,9 @@ unsigned* device_error_word();
 
 // Encodes a 2-D tiled tensor map over a pool viewed as rows of head_dim
 // elements: dims {head_dim, rows}, box {box_x, box_y}, 128-byte swizzle.
-pa_status encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int head_dim,
-                          uint64_t rows, int box_x, int box_y, bool swizzle128 = true);
+// swizzle: 0 none, 64 or 128 (bytes); row_elems = elements per row of the view
+pa_status encode_pool_map(CUtensorMap* map, const void* base, pa_dtype dt, int row_elems,
+                          uint64_t rows, int box_x, int box_y, int swizzle = 128);
 
 // Profiling events for the main decode kernel (may be null).
 void profile_events(cudaEvent_t* start, cudaEvent_t* stop);

@@ -70,7 +70,9 @@ class PagedStep:
         if self.fp8:
             self.k_cache = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8,
                                       device=dev).view(torch.float8_e4m3fn)
-            self.v_cache = self.k_cache.clone()
+            # FP8 V codes are stored transposed per (block, head): [d][block_size]
+            self.v_cache = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8,
+                                      device=dev).view(torch.float8_e4m3fn)
         else:
             self.k_cache = torch.full((nb, n_kv, bs, d), float("nan"), dtype=wl.dtype, device=dev)
             self.v_cache = torch.full((nb, n_kv, bs, d), float("nan"), dtype=wl.dtype, device=dev)

@@ -32,7 +32,7 @@ def test_fp8_cache_write_whole_pool_bit_exact(act, scale):
     slots = np.random.default_rng(3).permutation(nb * bs)[:T].astype(np.int64)
     slots[5] = -1                                               # padding token
     kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
-    vc = kc.clone()
+    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
     pa.pa_reshape_and_cache_quant(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(slots).cuda(),
                                   k_scale=scale, v_scale=scale)
     torch.cuda.synchronize()
@@ -40,7 +40,9 @@ def test_fp8_cache_write_whole_pool_bit_exact(act, scale):
     kq = torch.from_numpy(oracle.quantize_fp8(k, scale))
     vq = torch.from_numpy(oracle.quantize_fp8(v, scale))
     pool0 = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8)
-    ek, ev = oracle.cache_write(pool0, pool0, kq, vq, slots, bs)
+    ek, _ = oracle.cache_write(pool0, pool0, kq, vq, slots, bs)
+    # V codes land in the transposed layout [block][head][d][offset]
+    ev = oracle.cache_write_vt(torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8), vq, slots, bs)
     assert np.array_equal(kc.view(torch.uint8).cpu().numpy().reshape(-1), ek)
     assert np.array_equal(vc.view(torch.uint8).cpu().numpy().reshape(-1), ev)
 
