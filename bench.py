@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 # source is byte-identical to what was profiled (sha256 of csrc/decode.cu).
 NCU_TRAFFIC = {
     # ncu --set full on a 64-sequence case of the same shapes, scaled by unique
-    # K/V bytes to the 256-sequence workload (see profiles/decode_mma_llama3-8b-bf16_b64_full.md)
-    ("llama3-8b-bf16", 256, "665d4727fef49309"): 2400196821,
+    # K/V bytes to the 256-sequence workload (profiles/decode_mma_llama3-8b-bf16_b64_full.md)
+    ("llama3-8b-bf16", 256, "1de313c840c68565"): 2402456678,
 }
 
 
@@ -142,12 +142,16 @@ def oracle_sample(wl_name: str, n_seqs: int | None, target_s: float, seed_offset
     prefix = dr.prefix_kv() if sharers.any() else None
     q_all = dr.q()
     threads = oracle.default_threads()
-    row = 2 * wl.n_kv_heads * wl.head_dim * wl.elem_bytes
+    row = 2 * wl.n_kv_heads * wl.head_dim * wl.pool_elem_bytes
+    fp8 = wl.cache_dtype is not None
 
     def run(seqs):
         ks, vs = [], []
         for s in seqs:
             k, v = dr.seq_kv(s, int(lens[s]), bool(sharers[s]), prefix)
+            if fp8:   # the pool holds E4M3 codes: the oracle reads their values
+                k = oracle.dequantize_fp8(oracle.quantize_fp8(k, wl.kv_scale), wl.kv_scale)
+                v = oracle.dequantize_fp8(oracle.quantize_fp8(v, wl.kv_scale), wl.kv_scale)
             ks.append(k); vs.append(v)
         t0 = time.perf_counter()
         oracle.decode(q_all[seqs], ks, vs, wl.scale, threads=threads)
@@ -330,7 +334,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"torch.bfloat16": "bf16", "torch.float16": "f16", "torch.float32": "f32"}[str(wl.dtype)],
+        "dtype": ("e4m3 K/V, f16 products" if wl.cache_dtype is not None else
+                  {"torch.bfloat16": "bf16", "torch.float16": "f16", "torch.float32": "f32"}[str(wl.dtype)]),
         "data": "synthetic (seeded N(0,1) K/V/Q, random block scatter)",
         "config": {"workload": wl.name, "batch": B, "n_q_heads": wl.n_q_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
