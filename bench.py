@@ -77,6 +77,24 @@ def _cores() -> int:
     return len(os.sched_getaffinity(0))
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(vals, device="cpu"):
+    """Element-wise max of per-rank values over all ranks (timings: the job is
+    as slow as its slowest replica).  No-op on a single process."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank processes its own batch of the same size, so the
+    job moves world x bytes_per_rank per step of the slowest rank."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -315,15 +333,11 @@ def run_ours(args, rank, world, local_rank):
     # ---- reductions over ranks (max time) --------------------------------
     ms_step = ms_total / args.steps
     dec_ms = statistics.mean(decode_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step, e2e_ms, dec_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms, dec_ms = (float(x) for x in t.tolist())
+    ms_step, e2e_ms, dec_ms = max_over_ranks([ms_step, e2e_ms, dec_ms], dev)
 
     kv_unique = st.kv_bytes_unique()
     kv_logical = st.kv_bytes_logical()
-    value = world * kv_unique / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(kv_unique, world, ms_step)
     peak, peak_kind = _peaks()
     # algorithmic bytes of the main decode kernel per launch: the unique K/V
     # bytes plus q, the output/partials are < 0.5% and not counted
@@ -350,7 +364,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": tr,
                      "kernel": "decode_mma_kernel", "peak_source": f"hbm_gbs ({peak_kind})"},
-        "e2e": {"value": world * kv_unique / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": whole_job_gbs(kv_unique, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

@@ -235,6 +235,13 @@ const char* pa_status_string(pa_status status);
 /* Text of the last host-side failure on the calling thread ("" if none). */
 const char* pa_last_error_message(void);
 
+/* Self-test of the bounded waits: launches one thread that waits on an
+ * mbarrier nothing ever completes.  After limit_us (1 .. 2e6) the wait gives up,
+ * PA_ERR_TIMEOUT is recorded in the device error word and the kernel writes 2
+ * to *scratch (a device word) and returns; the context stays usable.  Read the
+ * outcome with pa_get_device_error. */
+pa_status pa_selftest_bounded_wait(unsigned limit_us, void* scratch, void* stream);
+
 /* Measurement hook: when both are non-NULL, pa_decode records `start` right
  * before its main attention kernel and `stop` right after it on the call's
  * stream (cudaEvent_t passed as void*).  Pass NULL, NULL to turn it off. */

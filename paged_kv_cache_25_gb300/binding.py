@@ -49,6 +49,7 @@ _SIGS = {
     "pa_copy_blocks": (I, [P, P, C.POINTER(_Desc), P, I, P]),
     "pa_swap_blocks": (I, [P, P, I, P, P, I, C.POINTER(_Desc), P, I, P]),
     "pa_get_device_error": (I, [P]),
+    "pa_selftest_bounded_wait": (I, [C.c_uint, P, P]),
     "pa_status_string": (C.c_char_p, [I]),
     "pa_last_error_message": (C.c_char_p, []),
     "pa_set_profile_events": (None, [P, P]),
@@ -236,6 +237,12 @@ def pa_swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping, stream=None):
 def pa_get_device_error(stream=None) -> int:
     """Synchronizes the stream, returns and clears the device error word."""
     return int(lib().pa_get_device_error(_stream(stream)))
+
+
+def pa_selftest_bounded_wait(limit_us: int, scratch, stream=None):
+    """Run the bounded-wait self-test (a wait nothing completes) on `stream`."""
+    _check(lib().pa_selftest_bounded_wait(int(limit_us), _ptr(scratch), _stream(stream)),
+           "pa_selftest_bounded_wait")
 
 
 def pa_set_profile_events(start=None, stop=None):

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -164,6 +165,18 @@ static size_t decode_ws_bytes(int B, int n_q, int n_kv, int D, int BS, int max_c
     return kControlBytes + align256(units * 2 * sizeof(float)) + units * D * sizeof(float);
 }
 
+// One thread waits on an mbarrier that nothing ever completes: the bounded
+// wait gives up after limit_ns, records PA_ERR_TIMEOUT and the kernel returns.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned* err, unsigned* reached)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    const bool ok = mbar_wait(b, 0, err, limit_ns);
+    *reached = ok ? 1u : 2u;   // 2: the wait ran out and the kernel went on
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -190,6 +203,21 @@ void pa_set_profile_events(void* start, void* stop)
 {
     g_prof_start.store(static_cast<cudaEvent_t>(start));
     g_prof_stop.store(static_cast<cudaEvent_t>(stop));
+}
+
+pa_status pa_selftest_bounded_wait(unsigned limit_us, void* scratch, void* stream)
+{
+    if (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 3u) != 0)
+        return fail(PA_ERR_INVALID_ARG, "scratch must be a 4-byte aligned device word");
+    if (limit_us == 0 || limit_us > 2000000u)
+        return fail(PA_ERR_INVALID_ARG, "limit_us must be in [1, 2e6]");
+    unsigned* err = device_error_word();
+    if (!err) return fail(PA_ERR_CUDA, "cannot locate the device error word");
+    selftest_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint64_t>(limit_us) * 1000u, err, static_cast<unsigned*>(scratch));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return ok();
 }
 
 pa_status pa_get_device_error(void* stream)

@@ -89,14 +89,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records PA_ERR_TIMEOUT) if it has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err)
+// records PA_ERR_TIMEOUT) if it has not completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_test_wait(bar, parity)) return true;      // already complete: no suspend
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) {
             set_error(err, PA_ERR_TIMEOUT);
             return false;
         }
