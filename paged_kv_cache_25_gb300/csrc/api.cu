@@ -107,11 +107,12 @@ void profile_events(cudaEvent_t* start, cudaEvent_t* stop)
 // ------------------------------------------------------------------ partition policy
 int decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int max_context_len)
 {
-    // 512 tokens (32 or 16 blocks) per partition keeps the split-K overhead at
-    // a few percent of the K/V bytes; halve it (down to 128) while the batch
-    // would offer fewer than ~8 units of work per resident CTA (2 per SM on
-    // 152 SMs).
-    int p = 512;
+    // 1024 tokens (64 or 32 blocks) per partition spreads the fixed cost of a
+    // unit (block ids, q fragments, the first TMA round trip, the cross-warp
+    // combine) over 16 stages per warp and keeps the split-K bytes below 1 %;
+    // halve it (down to 128) while the batch would offer fewer than ~8 units
+    // of work per resident CTA (2 per SM on 152 SMs).
+    int p = 1024;
     while (p > 128 && p > block_size &&
            static_cast<int64_t>(num_seqs) * n_kv_heads * ((max_context_len + p - 1) / p) < 2432)
         p /= 2;

@@ -203,6 +203,28 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int blk0 = tok0 / BS;
         const int nparts = min((L + part_tokens - 1) / part_tokens, max_parts);
 
+        // query fragments (issued before the block-id barrier so their latency
+        // overlaps it): rows 0-7 = heads of the sub-group, rows 8-15 zero
+        uint32_t qa[D / 16][2];
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            if (g < nh) {
+                if constexpr (FP8) {
+                    // k order of the FP8 fragments: columns 4*t4 .. 4*t4+3 of the chunk
+                    const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 4 * t4;
+                    qa[kk][0] = q_pair<QT, T>(qp);
+                    qa[kk][1] = q_pair<QT, T>(qp + 2);
+                } else {
+                    const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
+                    qa[kk][0] = q_pair<QT, T>(qp);
+                    qa[kk][1] = q_pair<QT, T>(qp + 8);
+                }
+            } else {
+                qa[kk][0] = 0u;
+                qa[kk][1] = 0u;
+            }
+        }
+
         // block ids of the partition, range-checked before any load is issued
         int bad = 0;
         for (int i = tid; live && i < nblk; i += kDecWarps * 32) {
@@ -248,27 +270,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (lane == 0) {
             fence_proxy_async_smem();
             for (int k = 0; k < min(NS, my_n); ++k) issue(k);
-        }
-
-        // query fragments: rows 0-7 = heads of the sub-group, rows 8-15 zero
-        uint32_t qa[D / 16][2];
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            if (g < nh) {
-                if constexpr (FP8) {
-                    // k order of the FP8 fragments: columns 4*t4 .. 4*t4+3 of the chunk
-                    const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 4 * t4;
-                    qa[kk][0] = q_pair<QT, T>(qp);
-                    qa[kk][1] = q_pair<QT, T>(qp + 2);
-                } else {
-                    const QT* qp = q + (static_cast<int64_t>(s) * n_q + h0 + g) * D + kk * 16 + 2 * t4;
-                    qa[kk][0] = q_pair<QT, T>(qp);
-                    qa[kk][1] = q_pair<QT, T>(qp + 8);
-                }
-            } else {
-                qa[kk][0] = 0u;
-                qa[kk][1] = 0u;
-            }
         }
 
         float o[D / 8][4];

@@ -115,6 +115,23 @@ def test_decode_edge_shapes(case):
     assert err <= TOL[dtype], err
 
 
+def test_decode_1024_token_partitions_all_outputs():
+    """A batch large enough for the widest partitions (64 sequences x 8 KV heads
+    x 5 partitions of the longest context = 2560 units >= 8 per resident CTA):
+    lengths on every 1024-token edge, plus a ragged spread, all outputs checked."""
+    edges = [1, 15, 16, 17, 1023, 1024, 1025, 2047, 2048, 2049, 3071, 4096, 4097, 5000]
+    rng = np.random.default_rng(77)
+    lens = edges + [int(x) for x in rng.integers(1, 5001, size=64 - len(edges))]
+    wl = _small(41, 64, 32, 8, 128, 16, torch.bfloat16, lens)
+    st = PagedStep(wl, out_dtype=torch.float32)
+    st.step()
+    torch.cuda.synchronize()
+    _check_clean()
+    ref = oracle_decode(st)
+    err = max_err(st.out, ref)
+    assert err <= TOL[torch.bfloat16], err
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_decode_low_precision_output(dtype):
     wl = _small(21, 4, 32, 8, 128, 16, dtype, [20, 300, 1024, 3000])

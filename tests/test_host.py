@@ -134,9 +134,9 @@ def test_workspace_size_rules():
     # a single partition needs only the 256-byte control area
     assert pa.pa_decode_workspace_size(256, 32, 8, 128, 16, 16) == 256
     w = pa.pa_decode_workspace_size(256, 32, 8, 128, 16, 4096)
-    assert w >= 256 * 32 * 8 * 128 * 4      # at least 8 partitions of fp32 partial outputs
+    assert w >= 256 * 32 * 4 * 128 * 4      # at least 4 partitions of fp32 partial outputs
     assert pa.pa_decode_workspace_size(0, 32, 8, 128, 16, 4096) == 0
-    # partitions shrink (512 -> 128 tokens) when a batch offers little work
+    # partitions shrink (1024 -> 128 tokens) when a batch offers little work
     small = pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 4096)
     assert small >= 256 + 4 * 32 * 32 * 128 * 4
 
