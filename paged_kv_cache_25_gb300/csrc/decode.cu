@@ -68,10 +68,15 @@ struct DecodeCfg {
 };
 
 // E4M3 pair -> fp16 pair (exact: every E4M3 value is an fp16 value)
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v)
+// Four E4M3 codes (one fragment word) widened exactly to two f16x2 words:
+// lo = codes 0,1 and hi = codes 2,3, each in its original order.
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
 template <typename QT, typename T>
@@ -326,7 +331,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         for (int jj = 0; jj < 4; ++jj) {
                             const int kk = kq * 4 + jj;
                             const uint32_t a[4] = {qa[kk][0], 0u, qa[kk][1], 0u};
-                            MmaOp<T>::run(sc[nt], a, e4m3x2_to_h2(w[jj] & 0xFFFF), e4m3x2_to_h2(w[jj] >> 16));
+                            uint32_t b0, b1;
+                            e4m3x4_to_h2x2(w[jj], b0, b1);
+                            MmaOp<T>::run(sc[nt], a, b0, b1);
                         }
                     }
                 }
@@ -377,22 +384,28 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const float m_new = fmaxf(m_run, mx);
-            const float alpha = exp2f(m_run - m_new);
+            // rescale only when some row's running max moved (warp-uniform
+            // branch; after the first stages the max rarely moves).  The first
+            // stage has m_run = -inf: alpha = 0 clears the (zero) state.
+            if (__any_sync(0xffffffffu, m_new != m_run)) {
+                const float alpha = fast_exp2(m_run - m_new);
+                l_run *= alpha;
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) {
+                    o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha; o[i][3] *= alpha;
+                }
+            }
             m_run = m_new;
             float psum = 0.f;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const float p = exp2f(sc[nt][e] - m_new);
+                    const float p = fast_exp2(sc[nt][e] - m_new);
                     sc[nt][e] = p;
                     psum += p;
                 }
-            l_run = l_run * alpha + psum;
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha; o[i][3] *= alpha;
-            }
+            l_run += psum;
 
             // O += P V, P as hi (rows 0-7) + lo (rows 8-15)
             uint32_t pa[4];
@@ -408,7 +421,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     ldsm_x4(vbase + d_row * 16, w[0], w[1], w[2], w[3]);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
-                        MmaOp<T>::run(o[nd + jj], pa, e4m3x2_to_h2(w[jj] & 0xFFFF), e4m3x2_to_h2(w[jj] >> 16));
+                    {
+                        uint32_t b0, b1;
+                        e4m3x4_to_h2x2(w[jj], b0, b1);
+                        MmaOp<T>::run(o[nd + jj], pa, b0, b1);
+                    }
                 }
             } else {
 #pragma unroll
