@@ -286,6 +286,58 @@ pa_status pa_slot_mapping(const int32_t* tables, int max_blocks_per_seq, int blo
                           const int32_t* seq, const int32_t* pos, int num_tokens,
                           int64_t* slots);
 
+/* ---------------------------------------------------------------- prefix cache
+ * Automatic reuse of computed K/V blocks across requests ("The hands-on guide
+ * to LLM Inference with vLLM", Automatic Prefix Caching; "vLLM Serving ...",
+ * "Prefix caching (automatic KV reuse)"; "Inference engineering", Trick 3):
+ *  - only full blocks are cached; a block's fingerprint chains the fingerprint
+ *    of the block before it (0 for the first) with its block_size token ids:
+ *    FNV-1a 64 over the parent (8 bytes, little endian), then each token id
+ *    (4 bytes, little endian).  An entry also keeps the parent fingerprint and
+ *    the tokens, so a hit always means equal contents;
+ *  - a request reuses the leading run of its full blocks that hit; every block
+ *    counts the requests using it;
+ *  - a block whose count drops to zero keeps its entry on an LRU list; new
+ *    blocks come from the free queue first and, only when it is empty, by
+ *    evicting the least recently released cached block (blocks released in
+ *    one call count as released deepest first).
+ * Host memory only; not thread-safe (one owner thread).  Block ids are the
+ * pool's physical blocks, the same ids pa_decode's tables hold. */
+typedef struct pa_prefix pa_prefix;
+/* free_order: the free queue's starting order (a permutation of
+ * 0..num_blocks-1) or NULL.  Returns NULL on bad arguments. */
+pa_prefix* pa_prefix_create(int num_blocks, int block_size, const int32_t* free_order);
+void pa_prefix_destroy(pa_prefix* p);
+/* Fingerprint of one full block of block_size tokens after `parent`. */
+uint64_t pa_prefix_block_hash(uint64_t parent, const int32_t* tokens, int block_size);
+/* Number of leading full blocks of tokens[0..n_tokens) already cached (no
+ * change to the cache), or -1 on bad arguments. */
+int pa_prefix_lookup(const pa_prefix* p, const int32_t* tokens, int n_tokens);
+/* Block table for a request of n_tokens >= 1 tokens: its hitting leading full
+ * blocks (one more reference each), then ceil(n_tokens / block_size) - hits
+ * new blocks; entries past those up to table_len are set to -1.  Returns the
+ * number of hit blocks (their K/V need not be recomputed), -1 when the pool
+ * cannot supply the new blocks (nothing taken), -2 on bad arguments. */
+int pa_prefix_acquire(pa_prefix* p, const int32_t* tokens, int n_tokens, int32_t* table,
+                      int table_len);
+/* n more blocks for growing sequences (reference count 1 each).  Returns 0,
+ * -1 when the pool cannot supply them (nothing taken), -2 on bad arguments. */
+int pa_prefix_alloc(pa_prefix* p, int n, int32_t* out);
+/* Registers the full blocks of a request whose K/V have been written: for
+ * block i < n_tokens / block_size, table[i] is entered unless the same
+ * contents are cached already (then table[i] stays private).  Every listed
+ * full block must be held (count > 0).  Returns the number of blocks entered,
+ * or -2 on bad arguments (nothing entered). */
+int pa_prefix_commit(pa_prefix* p, const int32_t* tokens, int n_tokens, const int32_t* table);
+/* Drops one reference from each listed block (-1 entries skipped).  Returns 0,
+ * or -2 (nothing changed) on an id out of range or a block without enough
+ * references. */
+int pa_prefix_release(pa_prefix* p, const int32_t* table, int n_blocks);
+int pa_prefix_num_free(const pa_prefix* p);       /* free, not cached */
+int pa_prefix_num_evictable(const pa_prefix* p);  /* cached, count 0 */
+int pa_prefix_num_cached(const pa_prefix* p);     /* entries in the table */
+int pa_prefix_refcount(const pa_prefix* p, int block);
+
 /* Sizing ("vLLM Serving ...", "How big is the KV cache?"):
  * 2 * n_layers * n_kv_heads * head_dim * elem_bytes, and the number of whole
  * blocks of block_size tokens that fit in pool_bytes. */

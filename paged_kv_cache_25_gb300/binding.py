@@ -21,7 +21,7 @@ __all__ = [
     "pa_decode_workspace_size",
     "pa_decode_no_alloc", "PA_DECODE_NO_ALLOC_SCRATCH_BYTES",
     "pa_prefill_chunk", "pa_prefill_workspace_size", "pa_get_device_error", "pa_status_string",
-    "pa_set_profile_events", "pa_copy_blocks", "pa_swap_blocks", "Allocator", "pa_slot_mapping", "pa_kv_bytes_per_token",
+    "pa_set_profile_events", "pa_copy_blocks", "pa_swap_blocks", "Allocator", "PrefixCache", "pa_prefix_block_hash", "pa_slot_mapping", "pa_kv_bytes_per_token",
     "pa_pool_blocks", "EXPORTED", "dtype_code",
 ]
 
@@ -62,6 +62,18 @@ _SIGS = {
     "pa_alloc_destroy": (None, [P]),
     "pa_alloc_build_tables": (I, [P, I, P, P, I, I, I, P]),
     "pa_slot_mapping": (I, [P, I, I, P, P, I, P]),
+    "pa_prefix_create": (P, [I, I, P]),
+    "pa_prefix_destroy": (None, [P]),
+    "pa_prefix_block_hash": (C.c_uint64, [C.c_uint64, P, I]),
+    "pa_prefix_lookup": (I, [P, P, I]),
+    "pa_prefix_acquire": (I, [P, P, I, P, I]),
+    "pa_prefix_alloc": (I, [P, I, P]),
+    "pa_prefix_commit": (I, [P, P, I, P]),
+    "pa_prefix_release": (I, [P, P, I]),
+    "pa_prefix_num_free": (I, [P]),
+    "pa_prefix_num_evictable": (I, [P]),
+    "pa_prefix_num_cached": (I, [P]),
+    "pa_prefix_refcount": (I, [P, I]),
     "pa_kv_bytes_per_token": (L, [I, I, I, I]),
     "pa_pool_blocks": (L, [L, I, L]),
 }
@@ -296,6 +308,78 @@ class Allocator:
         h, self._h = getattr(self, "_h", None), None
         if h:
             self._l.pa_alloc_destroy(h)
+
+
+class PrefixCache:
+    """The library's host prefix cache: fingerprinted full blocks reused across
+    requests, unused cached blocks evicted least recently released first."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self._l = lib()
+        order = None if free_order is None else np.ascontiguousarray(free_order, np.int32)
+        self._h = self._l.pa_prefix_create(num_blocks, block_size, _ptr(order))
+        if not self._h:
+            raise PAError(PA_ERR_INVALID_ARG, "pa_prefix_create: bad size or order")
+        self.block_size = block_size
+
+    @staticmethod
+    def _toks(tokens):
+        return np.ascontiguousarray(tokens, np.int32)
+
+    def lookup(self, tokens) -> int:
+        t = self._toks(tokens)
+        return int(self._l.pa_prefix_lookup(self._h, _ptr(t), len(t)))
+
+    def acquire(self, tokens, table_len: int):
+        """(hit blocks, table) or None when the pool cannot supply the rest."""
+        t = self._toks(tokens)
+        table = np.empty(max(table_len, 1), np.int32)
+        r = self._l.pa_prefix_acquire(self._h, _ptr(t), len(t), _ptr(table), table_len)
+        if r == -2:
+            raise PAError(PA_ERR_INVALID_ARG, "pa_prefix_acquire: bad arguments")
+        return None if r < 0 else (int(r), table[:table_len])
+
+    def alloc(self, n: int):
+        out = np.empty(max(n, 1), np.int32)
+        r = self._l.pa_prefix_alloc(self._h, n, _ptr(out))
+        if r == -2:
+            raise PAError(PA_ERR_INVALID_ARG, "pa_prefix_alloc: bad arguments")
+        return None if r < 0 else out[:n]
+
+    def commit(self, tokens, table) -> int:
+        t = self._toks(tokens)
+        tb = np.ascontiguousarray(table, np.int32)
+        r = self._l.pa_prefix_commit(self._h, _ptr(t), len(t), _ptr(tb))
+        if r < 0:
+            raise PAError(PA_ERR_INVALID_ARG, "pa_prefix_commit: bad table")
+        return int(r)
+
+    def release(self, table):
+        tb = np.ascontiguousarray(table, np.int32)
+        if self._l.pa_prefix_release(self._h, _ptr(tb), len(tb)) != 0:
+            raise PAError(PA_ERR_INVALID_ARG, "pa_prefix_release: bad ids or counts")
+
+    def num_free(self) -> int:
+        return int(self._l.pa_prefix_num_free(self._h))
+
+    def num_evictable(self) -> int:
+        return int(self._l.pa_prefix_num_evictable(self._h))
+
+    def num_cached(self) -> int:
+        return int(self._l.pa_prefix_num_cached(self._h))
+
+    def refcount(self, block_id: int) -> int:
+        return int(self._l.pa_prefix_refcount(self._h, block_id))
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._l.pa_prefix_destroy(h)
+
+
+def pa_prefix_block_hash(parent: int, tokens) -> int:
+    t = np.ascontiguousarray(tokens, np.int32)
+    return int(lib().pa_prefix_block_hash(parent, _ptr(t), len(t)))
 
 
 def pa_slot_mapping(tables, block_size: int, seq, pos) -> np.ndarray:

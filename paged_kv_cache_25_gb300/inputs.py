@@ -46,7 +46,7 @@ import torch
 __all__ = ["Workload", "WORKLOADS", "get", "Draws"]
 
 _TAGS = {"lens": 1, "kv": 2, "q": 3, "order": 4, "share": 5, "prefix": 6,
-         "pq": 7, "pkv": 8, "plens": 9, "newkv": 10}
+         "pq": 7, "pkv": 8, "plens": 9, "newkv": 10, "toks": 11, "tokkv": 12}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -245,3 +245,21 @@ def random_case(seed: int, batch: int, n_q: int, n_kv: int, d: int, bs: int, dty
     return Workload(f"case-{seed}", seed, batch, n_q, n_kv, d, bs, dtype, std=std,
                     lens_kind="list", lens_args=tuple(int(x) for x in lens),
                     cache_dtype=cache_dtype, kv_scale=kv_scale)
+
+
+def token_stream(seed: int, index: int, length: int, vocab: int) -> np.ndarray:
+    """Token ids of one synthetic request (uniform over the vocabulary)."""
+    return _rng(seed, "toks", index).integers(0, vocab, size=length).astype(np.int32)
+
+
+def token_keyed_kv(seed: int, tokens, n_kv: int, head_dim: int, dtype, std: float = 1.0):
+    """K and V rows [len][n_kv][d] for a token sequence where the row at
+    position p is drawn from a generator keyed by tokens[0..p] only: requests
+    that share a prefix of tokens get identical rows over that prefix."""
+    ks, vs = [], []
+    toks = [int(t) for t in tokens]
+    for p in range(len(toks)):
+        r = np.random.default_rng([seed, _TAGS["tokkv"], p, *toks[:p + 1]])
+        ks.append(_normal(r, (n_kv, head_dim), std, dtype))
+        vs.append(_normal(r, (n_kv, head_dim), std, dtype))
+    return torch.stack(ks), torch.stack(vs)
