@@ -149,6 +149,34 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q,
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int n_kv_heads, int head_dim,
                                 int block_size, int max_context_len);
 
+/* ---------------------------------------------------------------- multi-query decode
+ * Verification of k drafted tokens in one pass ("vLLM Serving ...",
+ * "Speculative decoding"; "Inference engineering", Trick 5: the target model
+ * checks all k guesses in one forward pass): every sequence brings q_per_seq
+ * = k + 1 query rows whose K/V rows were appended first, so
+ *   out[s][i][h] = softmax(scale * q[s][i][h] . K_s[0..p]^T) V_s[0..p],
+ *   p = context_lens[s] - q_per_seq + i      (causal among the new rows).
+ * The g query heads of a KV head and the q_per_seq rows form (head, query)
+ * rows of one tensor-core tile, so each K/V slab is still read once for all
+ * of them.
+ *   out, q       : [num_seqs][q_per_seq][n_q_heads][head_dim] (out in out_dtype,
+ *                  q in the cache dtype, or cache->act_dtype for FP8 pools).
+ *   context_lens : include the q_per_seq new rows; a length below q_per_seq
+ *                  flags PA_ERR_OUT_OF_RANGE in the device error word and the
+ *                  sequence's rows are not written.
+ *   workspace    : pa_decode_verify_workspace_size(...) bytes, as for pa_decode.
+ * q_per_seq in [1, 16]; q_per_seq = 1 is pa_decode.  bf16/fp16/FP8 pools with
+ * head_dim 64 or 128 (else PA_ERR_UNSUPPORTED); other rules as pa_decode. */
+pa_status pa_decode_verify(void* out, pa_dtype out_dtype, const void* q,
+                           const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int q_per_seq,
+                           int n_q_heads, float scale, int block_size,
+                           void* workspace, size_t workspace_bytes, void* stream);
+size_t pa_decode_verify_workspace_size(int num_seqs, int q_per_seq, int n_q_heads,
+                                       int n_kv_heads, int head_dim, int block_size,
+                                       int max_context_len);
+
 /* ---------------------------------------------------------------- decode, no allocation
  * The paper has no counterpart to this call.  It is pa_decode for callers that
  * cannot allocate device memory: a host runtime that gives all free HBM to its

@@ -18,7 +18,7 @@ from . import build as _build
 
 __all__ = [
     "PAError", "lib", "pa_reshape_and_cache", "pa_reshape_and_cache_quant", "pa_decode",
-    "pa_decode_workspace_size",
+    "pa_decode_workspace_size", "pa_decode_verify", "pa_decode_verify_workspace_size",
     "pa_decode_no_alloc", "PA_DECODE_NO_ALLOC_SCRATCH_BYTES",
     "pa_prefill_chunk", "pa_prefill_workspace_size", "pa_get_device_error", "pa_status_string",
     "pa_set_profile_events", "pa_copy_blocks", "pa_swap_blocks", "Allocator", "PrefixCache", "pa_prefix_block_hash", "pa_slot_mapping", "pa_kv_bytes_per_token",
@@ -43,6 +43,8 @@ _SIGS = {
     "pa_decode": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, F, I, P, SZ, P]),
     "pa_decode_workspace_size": (SZ, [I, I, I, I, I, I]),
     "pa_decode_no_alloc": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, F, I, P]),
+    "pa_decode_verify": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, I, I, I, F, I, P, SZ, P]),
+    "pa_decode_verify_workspace_size": (SZ, [I, I, I, I, I, I, I]),
     "pa_reshape_and_cache_quant": (I, [P, P, I, P, P, P, I, C.POINTER(_Desc), P]),
     "pa_prefill_chunk": (I, [P, I, P, P, P, C.POINTER(_Desc), P, I, P, P, I, I, I, F, I, P, SZ, P]),
     "pa_prefill_workspace_size": (SZ, [I, I, I, I]),
@@ -165,6 +167,26 @@ def pa_decode_workspace_size(num_seqs, n_q_heads, n_kv_heads, head_dim, block_si
                              max_context_len) -> int:
     return int(lib().pa_decode_workspace_size(num_seqs, n_q_heads, n_kv_heads, head_dim,
                                               block_size, max_context_len))
+
+
+def pa_decode_verify_workspace_size(num_seqs, q_per_seq, n_q_heads, n_kv_heads, head_dim,
+                                    block_size, max_context_len) -> int:
+    return int(lib().pa_decode_verify_workspace_size(num_seqs, q_per_seq, n_q_heads, n_kv_heads,
+                                                     head_dim, block_size, max_context_len))
+
+
+def pa_decode_verify(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                     block_size: int, workspace=None, stream=None, k_scale=None, v_scale=None):
+    """out, q [B][q_per_seq][n_q][d]: query i of sequence s sits at position
+    context_lens[s] - q_per_seq + i and sees keys up to it."""
+    B, nq, n_q, _ = q.shape
+    d = _desc(k_cache, k_scale, v_scale, q.dtype)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().pa_decode_verify(_ptr(out), dtype_code(out.dtype), _ptr(q), _ptr(k_cache),
+                                  _ptr(v_cache), C.byref(d), _ptr(block_tables),
+                                  int(block_tables.shape[1]), _ptr(context_lens), int(B), int(nq),
+                                  int(n_q), float(scale), int(block_size), _ptr(workspace),
+                                  ws_bytes, _stream(stream)), "pa_decode_verify")
 
 
 def pa_reshape_and_cache_quant(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,

@@ -17,7 +17,7 @@ SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libpa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["api.cu", "cache_write.cu", "copy_blocks.cu", "decode.cu", "decode_no_alloc.cu", "prefill_tc.cu"]
+CUDA_SOURCES = ["api.cu", "cache_write.cu", "copy_blocks.cu", "decode.cu", "decode_verify.cu", "decode_no_alloc.cu", "prefill_tc.cu"]
 CXX_SOURCES = ["host_alloc.cpp", "prefix_cache.cpp"]
 
 

@@ -105,7 +105,7 @@ void profile_events(cudaEvent_t* start, cudaEvent_t* stop)
 }
 
 // ------------------------------------------------------------------ partition policy
-int decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int max_context_len)
+int decode_partition_tokens(int64_t seq_groups, int block_size, int max_context_len)
 {
     // 1024 tokens (64 or 32 blocks) per partition spreads the fixed cost of a
     // unit (block ids, q fragments, the first TMA round trip, the cross-warp
@@ -114,7 +114,7 @@ int decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int ma
     // of work per resident CTA (2 per SM on 152 SMs).
     int p = 1024;
     while (p > 128 && p > block_size &&
-           static_cast<int64_t>(num_seqs) * n_kv_heads * ((max_context_len + p - 1) / p) < 2432)
+           seq_groups * ((max_context_len + p - 1) / p) < 2432)
         p /= 2;
     return p;
 }
@@ -154,15 +154,17 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // partial outputs [B][n_q][J][D], all fp32.
 static constexpr size_t kControlBytes = 256;
 
-static size_t decode_ws_bytes(int B, int n_q, int n_kv, int D, int BS, int max_ctx, int* part,
-                              int* parts)
+static size_t decode_ws_bytes(int B, int nq, int n_q, int n_kv, int D, int BS, int max_ctx,
+                              int* part, int* parts)
 {
-    const int p = decode_partition_tokens(B, n_kv, BS, max_ctx);
+    // work units per partition index: (sequence, KV head, 8-row sub-group)
+    const int64_t groups = static_cast<int64_t>(B) * n_kv * ((n_q / n_kv * nq + 7) / 8);
+    const int p = decode_partition_tokens(groups, BS, max_ctx);
     const int J = (max_ctx + p - 1) / p;
     if (part) *part = p;
     if (parts) *parts = J < 1 ? 1 : J;
     if (J <= 1) return kControlBytes;
-    const size_t units = static_cast<size_t>(B) * n_q * J;
+    const size_t units = static_cast<size_t>(B) * nq * n_q * J;
     return kControlBytes + align256(units * 2 * sizeof(float)) + units * D * sizeof(float);
 }
 
@@ -329,15 +331,27 @@ size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int n_kv_heads, int
     if (num_seqs <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         max_context_len <= 0)
         return 0;
-    return decode_ws_bytes(num_seqs, n_q_heads, n_kv_heads, head_dim, block_size, max_context_len,
-                           nullptr, nullptr);
+    if (n_q_heads % n_kv_heads != 0) return 0;
+    return decode_ws_bytes(num_seqs, 1, n_q_heads, n_kv_heads, head_dim, block_size,
+                           max_context_len, nullptr, nullptr);
 }
 
-pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
-                    const void* v_cache, const pa_cache_desc* cache, const int32_t* block_tables,
-                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
-                    int n_q_heads, float scale, int block_size, void* workspace,
-                    size_t workspace_bytes, void* stream)
+size_t pa_decode_verify_workspace_size(int num_seqs, int q_per_seq, int n_q_heads, int n_kv_heads,
+                                       int head_dim, int block_size, int max_context_len)
+{
+    if (num_seqs <= 0 || q_per_seq <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || max_context_len <= 0 || n_q_heads % n_kv_heads != 0)
+        return 0;
+    return decode_ws_bytes(num_seqs, q_per_seq, n_q_heads, n_kv_heads, head_dim, block_size,
+                           max_context_len, nullptr, nullptr);
+}
+
+static pa_status decode_common(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                               const void* v_cache, const pa_cache_desc* cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int q_per_seq,
+                               int n_q_heads, float scale, int block_size, void* workspace,
+                               size_t workspace_bytes, void* stream)
 {
     pa_status st = check_cache(cache);
     if (st != PA_OK) return st;
@@ -366,8 +380,8 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_
 
     const int max_ctx = max_blocks_per_seq * block_size;
     int part = 0, parts = 0;
-    const size_t need = decode_ws_bytes(num_seqs, n_q_heads, cache->n_kv_heads, cache->head_dim,
-                                        block_size, max_ctx, &part, &parts);
+    const size_t need = decode_ws_bytes(num_seqs, q_per_seq, n_q_heads, cache->n_kv_heads,
+                                        cache->head_dim, block_size, max_ctx, &part, &parts);
     if (parts > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions per sequence");
     if (!workspace || workspace_bytes < need)
         return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -382,10 +396,11 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_
     a.k_cache = k_cache; a.v_cache = v_cache; a.cache = *cache;
     a.block_tables = block_tables; a.max_blocks = max_blocks_per_seq;
     a.context_lens = context_lens; a.num_seqs = num_seqs; a.n_q = n_q_heads; a.scale = scale;
+    a.q_per_seq = q_per_seq;
     a.part_tokens = part; a.max_parts = parts; a.err = err;
     a.ticket = static_cast<unsigned*>(workspace);
     if (need > kControlBytes) {
-        const size_t units = static_cast<size_t>(num_seqs) * n_q_heads * parts;
+        const size_t units = static_cast<size_t>(num_seqs) * q_per_seq * n_q_heads * parts;
         char* base = static_cast<char*>(workspace) + kControlBytes;
         a.ws_ml = reinterpret_cast<float*>(base);
         a.ws_acc = reinterpret_cast<float*>(base + align256(units * 2 * sizeof(float)));
@@ -393,6 +408,36 @@ pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_
     cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ok();
+}
+
+pa_status pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                    const void* v_cache, const pa_cache_desc* cache, const int32_t* block_tables,
+                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                    int n_q_heads, float scale, int block_size, void* workspace,
+                    size_t workspace_bytes, void* stream)
+{
+    return decode_common(out, out_dtype, q, k_cache, v_cache, cache, block_tables,
+                         max_blocks_per_seq, context_lens, num_seqs, 1, n_q_heads, scale,
+                         block_size, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_verify(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                           const void* v_cache, const pa_cache_desc* cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int q_per_seq,
+                           int n_q_heads, float scale, int block_size, void* workspace,
+                           size_t workspace_bytes, void* stream)
+{
+    pa_status st = check_cache(cache);
+    if (st != PA_OK) return st;
+    if (q_per_seq < 1 || q_per_seq > 16)
+        return fail(PA_ERR_INVALID_ARG, "q_per_seq %d outside [1, 16]", q_per_seq);
+    if (cache->dtype == PA_F32 || (cache->head_dim != 64 && cache->head_dim != 128))
+        return fail(PA_ERR_UNSUPPORTED,
+                    "multi-query decode runs on bf16/fp16/FP8 pools with head_dim 64 or 128");
+    return decode_common(out, out_dtype, q, k_cache, v_cache, cache, block_tables,
+                         max_blocks_per_seq, context_lens, num_seqs, q_per_seq, n_q_heads, scale,
+                         block_size, workspace, workspace_bytes, stream);
 }
 
 size_t pa_prefill_workspace_size(int num_reqs, int n_q_heads, int head_dim, int total_q)

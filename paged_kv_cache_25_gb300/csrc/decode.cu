@@ -1,613 +1,12 @@
 // Paged decode attention: one query row per (sequence, query head) against
 // the sequence's K/V read through its block table ("How the attention kernel
 // actually reads paged blocks": look the block up once, q.k against its keys,
-// softmax-weighted sum of its values).
-//
-// Work unit = (sequence s, KV head [8-head sub-group], partition j of
-// part_tokens tokens).  Long contexts are split into partitions whose (max,
-// sum, unnormalised output) are combined by decode_reduce_kernel; a sequence
-// that fits in one partition is finished by the partition kernel itself.
-//
-// Tensor-core path (bf16/fp16, head_dim 64/128, block 16/32), persistent:
-//   - a grid of (SMs x resident CTAs) walks a compact list of the live units:
-//     each CTA builds the prefix sum of partitions per sequence in shared
-//     memory and maps unit numbers to (sequence, partition, head group) by
-//     binary search, so skewed lengths cost no empty CTAs;
-//   - the g query heads sharing one KV head form the M rows of an m16n8k16
-//     MMA, so each K/V slab is read from HBM once for the whole group;
-//   - each warp owns a ring of NS stages of 16 K/V rows; lane 0 streams them
-//     with 2-D TMA tile loads (128-byte swizzle, so ldmatrix reads are bank
-//     conflict free); a 32-token block is two stages, so the ring and the
-//     occupancy do not depend on the block size;
-//   - online softmax in registers with quad shuffles;
-//   - P is split into hi + lo halves of the input type and placed in rows
-//     0-7 and 8-15 of the A operand, so P.V costs one MMA yet keeps ~16 bits
-//     of P (rows 8-15 would otherwise be padding).  Groups of more than 8 heads
-//     are handled as several 8-head sub-groups.
-// CUDA-core path (fp32, or shapes the tensor path does not cover): one warp
-// per query head, plain loads, fp32 FMA.
-#include <cuda_fp8.h>
-
-#include "pa_device.cuh"
-#include "pa_internal.h"
-
-#include <math.h>
-
-#include <mutex>
-#include <type_traits>
+// softmax-weighted sum of its values).  The tensor-core kernel lives in
+// decode_mma.cuh; this file holds the CUDA-core kernel (fp32 pools and other
+// head dims), the split-K reduce and the launch.
+#include "decode_mma.cuh"
 
 namespace pa {
-
-constexpr int kDecWarps = 4;
-constexpr int kRows = 16;            // K/V rows per pipeline stage
-constexpr int kMaxPartBlocks = 64;   // blocks per partition (part_tokens / block_size)
-constexpr int kPrefixCap = 2048;     // sequences whose partition prefix sum fits in smem
-
-__device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dtype dt)
-{
-    if (dt == PA_F32)
-        static_cast<float*>(out)[idx] = v;
-    else if (dt == PA_BF16)
-        static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
-    else
-        static_cast<__half*>(out)[idx] = __float2half_rn(v);
-}
-
-// Resident CTAs per SM: FP8 stages cost the same fragment work for half the
-// bytes, so that path is bound by per-warp latency and runs more warps.
-constexpr int decode_ctas_per_sm(bool fp8) { return fp8 ? 3 : 2; }
-constexpr int kSmemPerSm = 233472;    // 228 KB of shared memory per SM
-constexpr int kStaticSmem = 10240;    // bound on the kernel's static shared memory
-constexpr int kPreferSepRed = 1;      // give the combine its own buffer when it fits
-
-// Dynamic shared memory a CTA may use at the resident count above.
-constexpr int decode_dyn_avail(bool fp8)
-{
-    return kSmemPerSm / decode_ctas_per_sm(fp8) - 1024 /* reserved */ - kStaticSmem - 1024 /* align */;
-}
-
-// Ring depth per warp: about `budget` bytes of K+V in flight per warp, at least
-// 2 stages; when a separate combine buffer fits beside a ring of at least 2
-// stages, the ring is cut to what fits beside it.
-template <typename T, int D, bool FP8>
-constexpr int decode_stages()
-{
-    constexpr int stage = 2 * kRows * D * (FP8 ? 1 : static_cast<int>(sizeof(T)));
-    constexpr int budget = FP8 ? 12288 : 24576;
-    constexpr int ns = budget / stage > 2 ? budget / stage : 2;
-    constexpr int red = kDecWarps * 8 * (D + 2) * 4;
-    constexpr int fit = (decode_dyn_avail(FP8) - red) / (kDecWarps * stage);
-    return kPreferSepRed && fit >= 2 ? (fit < ns ? fit : ns) : ns;
-}
-
-// FP8 pools: a stage holds 16 rows of E4M3 K codes (swizzled rows of D bytes)
-// and the matching D x 16 tile of the transposed V codes.
-template <typename T, int D, int NS, bool FP8 = false>
-struct DecodeCfg {
-    static constexpr int kElem = FP8 ? 1 : static_cast<int>(sizeof(T));
-    static constexpr int kSlabBytes = kRows * D * kElem;    // 16 rows of K or V as stored
-    static constexpr int kStageBytes = 2 * kSlabBytes;
-    static constexpr int kWarpBytes = NS * kStageBytes;
-    static constexpr int kRingBytes = kDecWarps * kWarpBytes;
-    static constexpr int kReduceBytes = kDecWarps * 8 * (D + 2) * 4;
-    // the combine buffer sits after the rings when both fit, else it aliases them
-    static constexpr bool kSepRed =
-        kPreferSepRed && kRingBytes + kReduceBytes <= decode_dyn_avail(FP8);
-    static constexpr int kRedOffset = kSepRed ? kRingBytes : 0;
-    static constexpr int kDynBytes =
-        (kSepRed ? kRingBytes + kReduceBytes
-                 : (kRingBytes > kReduceBytes ? kRingBytes : kReduceBytes)) + 1024;
-    static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
-    static_assert(kMaxPartBlocks <= kDecWarps * 32, "one block id per thread");
-};
-
-// Four E4M3 codes (one fragment word) widened exactly (every E4M3 value is an
-// fp16 value) to two f16x2 words: lo = codes 0,1 and hi = codes 2,3.
-__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi)
-{
-    asm("{\n\t.reg .b16 a, b;\n\t"
-        "mov.b32 {a, b}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-        : "=r"(lo), "=r"(hi) : "r"(w));
-}
-
-template <typename QT, typename T>
-__device__ __forceinline__ uint32_t q_pair(const QT* p)
-{
-    return __ldg(reinterpret_cast<const unsigned int*>(p));   // q already in the MMA type
-}
-template <>
-__device__ __forceinline__ uint32_t q_pair<__nv_bfloat16, __half>(const __nv_bfloat16* p)
-{
-    const float2 f = Cvt<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const unsigned int*>(p)));
-    return Cvt<__half>::pack(f.x, f.y);
-}
-
-template <typename T, typename QT, int D, int BS, int NS, bool FP8>
-__global__ void __launch_bounds__(kDecWarps * 32, decode_ctas_per_sm(FP8))
-decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
-                  const int32_t* __restrict__ block_tables, int max_blocks,
-                  const int32_t* __restrict__ context_lens, int num_seqs, int n_q, int n_kv,
-                  int group, int num_blocks, float scale_log2, float v_scale,
-                  float* __restrict__ ws_ml, float* __restrict__ ws_acc, int part_tokens,
-                  int max_parts, unsigned* __restrict__ ticket, unsigned* err)
-{
-    using Cfg = DecodeCfg<T, D, NS, FP8>;
-    static_assert(!FP8 || std::is_same<T, __half>::value, "FP8 pools compute in fp16");
-    constexpr int kHalves = D / 64;           // 64-column halves (one 128-byte swizzled row each)
-    constexpr int kHalfTile = kRows * 128;
-    constexpr int kCPB = BS / kRows;          // stages per block
-    static_assert(BS % kRows == 0, "block_size must be a multiple of 16");
-
-    __shared__ int s_prefix[kPrefixCap];
-    __shared__ int s_scan[kDecWarps * 32];
-    __shared__ int s_blk[2][kMaxPartBlocks];   // this unit's and the next unit's block ids
-    __shared__ int s_total;
-    __shared__ long long s_next;
-    __shared__ __align__(8) uint64_t s_bar[kDecWarps * NS];
-    extern __shared__ uint8_t dyn_smem[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n_sub = (group + 7) >> 3;
-    const int n_groups = n_kv * n_sub;
-    const bool use_prefix = num_seqs <= kPrefixCap;
-
-    // ---- units: first every full partition, then every sequence's last one.
-    // The last partitions are the ragged, cheaper units, so handing them out
-    // last evens out the tail of the static round-robin assignment.
-    // s_prefix[s] = inclusive prefix sum of (partitions of s) - 1.
-    if (use_prefix) {
-        const int per = (num_seqs + kDecWarps * 32 - 1) / (kDecWarps * 32);
-        const int b0 = tid * per, b1 = min(num_seqs, b0 + per);
-        int local = 0;
-        for (int i = b0; i < b1; ++i) {
-            const int L = __ldg(context_lens + i);
-            const int p = L > 0 ? min((L + part_tokens - 1) / part_tokens, max_parts) - 1 : 0;
-            s_prefix[i] = p;
-            local += p;
-        }
-        s_scan[tid] = local;
-        __syncthreads();
-        if (tid == 0) {
-            int acc = 0;
-            for (int i = 0; i < kDecWarps * 32; ++i) {
-                const int v = s_scan[i];
-                s_scan[i] = acc;
-                acc += v;
-            }
-            s_total = acc;                  // full partitions
-        }
-        __syncthreads();
-        int run = s_scan[tid];
-        for (int i = b0; i < b1; ++i) {
-            run += s_prefix[i];
-            s_prefix[i] = run;
-        }
-    } else if (tid == 0) {
-        s_total = num_seqs * (max_parts - 1);
-    }
-    if (tid < kDecWarps * NS) mbar_init(smem_u32(&s_bar[tid]), 1);
-    fence_mbar_init();
-    __syncthreads();
-
-    const int n_full = s_total;
-    const int64_t units = (static_cast<int64_t>(n_full) + num_seqs) * n_groups;
-    const uint32_t ring = smem_u32(smem) + warp * Cfg::kWarpBytes;
-    const uint32_t bar0 = smem_u32(&s_bar[warp * NS]);
-    const int g = lane >> 2, t4 = lane & 3;
-    uint32_t kt = 0;   // stages this warp has consumed so far: its ring position and phase
-    if (lane == 0) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-    }
-
-    // Units are handed out dynamically: unit blockIdx.x first, then tickets
-    // from a counter that starts at zero for every launch.  Work for the next
-    // unit overlaps the current one: its ticket is drawn one unit ahead, its
-    // block ids are loaded (one per thread) while the current unit streams,
-    // its q fragments while the current unit's warps combine, and - when the
-    // combine buffer does not alias the rings - its first stages are issued
-    // before that combine.
-    struct Unit {
-        int s, part, L, tok0, kvh, h0, nh, nblk, nchunk, blk0, nparts;
-        bool live;
-    };
-    auto describe = [&](int64_t uu) {
-        Unit x{};
-        x.live = false;
-        if (uu >= units) return x;
-        const int gp = static_cast<int>(uu / n_groups);
-        const int grp = static_cast<int>(uu - static_cast<int64_t>(gp) * n_groups);
-        if (gp >= n_full) {                           // a sequence's last partition
-            x.s = gp - n_full;
-            const int Ls = __ldg(context_lens + x.s);
-            x.part = Ls > 0 ? min((Ls + part_tokens - 1) / part_tokens, max_parts) - 1 : 0;
-        } else if (use_prefix) {
-            int lo = 0, hi = num_seqs - 1;            // first s with prefix[s] > gp
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (s_prefix[mid] > gp) hi = mid; else lo = mid + 1;
-            }
-            x.s = lo;
-            x.part = gp - (lo ? s_prefix[lo - 1] : 0);
-        } else {
-            x.s = gp / (max_parts - 1);
-            x.part = gp - x.s * (max_parts - 1);
-        }
-        x.L = __ldg(context_lens + x.s);
-        x.tok0 = x.part * part_tokens;
-        x.live = x.tok0 < x.L;                        // same decision in every thread
-        x.kvh = grp / n_sub;
-        const int sub = grp - x.kvh * n_sub;
-        x.h0 = x.kvh * group + sub * 8;
-        x.nh = min(8, group - sub * 8);
-        const int tok1 = min(x.L, x.tok0 + part_tokens);
-        x.nblk = (tok1 - x.tok0 + BS - 1) / BS;
-        x.nchunk = (tok1 - x.tok0 + kRows - 1) / kRows;
-        x.blk0 = x.tok0 / BS;
-        x.nparts = min((x.L + part_tokens - 1) / part_tokens, max_parts);
-        return x;
-    };
-    // block id i of unit x (-1 if the table has no such entry), checked
-    // against the pool: a bad id flags the device error and drops the unit
-    auto load_id = [&](const Unit& x, int i, int& bad) {
-        const int lb = x.blk0 + i;
-        int b = -1;
-        if (lb < max_blocks) b = __ldg(block_tables + static_cast<int64_t>(x.s) * max_blocks + lb);
-        if (b < 0 || b >= num_blocks) {
-            bad = 1;
-            set_error(err, PA_ERR_OUT_OF_RANGE);
-        }
-        return b;
-    };
-    // query fragments of unit x: rows 0-7 = heads of the sub-group, rows 8-15 zero
-    uint32_t qa[D / 16][2];
-    auto load_q = [&](const Unit& x) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            if (g < x.nh) {
-                const QT* row = q + (static_cast<int64_t>(x.s) * n_q + x.h0 + g) * D + kk * 16;
-                if constexpr (FP8) {
-                    // k order of the FP8 fragments: columns 4*t4 .. 4*t4+3 of the chunk
-                    qa[kk][0] = q_pair<QT, T>(row + 4 * t4);
-                    qa[kk][1] = q_pair<QT, T>(row + 4 * t4 + 2);
-                } else {
-                    qa[kk][0] = q_pair<QT, T>(row + 2 * t4);
-                    qa[kk][1] = q_pair<QT, T>(row + 2 * t4 + 8);
-                }
-            } else {
-                qa[kk][0] = 0u;
-                qa[kk][1] = 0u;
-            }
-        }
-    };
-    // stage k of a unit (blk = its block ids, kvh_ its KV head) into this
-    // warp's ring slot (base + k) % NS
-    auto issue = [&](const int* blk, int kvh_, int k, uint32_t base) {
-        const int c = warp + k * kDecWarps;
-        const int b = blk[c / kCPB];
-        const uint32_t st = (base + k) % NS;
-        const uint32_t kdst = ring + st * Cfg::kStageBytes;
-        const uint32_t vdst = kdst + Cfg::kSlabBytes;
-        const uint32_t bar = bar0 + st * 8;
-        const int row = (b * n_kv + kvh_) * BS + (c % kCPB) * kRows;
-        mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
-        if constexpr (FP8) {
-            tma_load_2d(kdst, &kmap, 0, row, bar);                       // 16 rows x D codes
-            tma_load_2d(vdst, &vmap, (c % kCPB) * kRows, (b * n_kv + kvh_) * D, bar);  // D x 16
-        } else {
-#pragma unroll
-            for (int hx = 0; hx < kHalves; ++hx) {
-                tma_load_2d(kdst + hx * kHalfTile, &kmap, hx * 64, row, bar);
-                tma_load_2d(vdst + hx * kHalfTile, &vmap, hx * 64, row, bar);
-            }
-        }
-    };
-    auto my_stages = [&](const Unit& x) {
-        return x.nchunk > warp ? (x.nchunk - warp + kDecWarps - 1) / kDecWarps : 0;
-    };
-
-    float* red_o = reinterpret_cast<float*>(smem + Cfg::kRedOffset);   // [warps][8][D]
-    float* red_m = red_o + kDecWarps * 8 * D;                           // [warps][8]
-    float* red_l = red_m + kDecWarps * 8;                               // [warps][8]
-
-    // ---- the first unit: ids checked before any load is issued
-    int64_t u = blockIdx.x;
-    if (u >= units) return;                           // uniform over the CTA
-    Unit cu = describe(u);
-    {
-        int bad = 0;
-        if (cu.live && tid < cu.nblk) s_blk[0][tid] = load_id(cu, tid, bad);
-        load_q(cu);
-        const int any_bad = __syncthreads_or(bad);
-        if (tid == 0) s_next = static_cast<long long>(gridDim.x) + atomicAdd(ticket, 1u);
-        cu.live = cu.live && !any_bad;
-        __syncthreads();
-    }
-    int64_t un = s_next;
-    int cb = 0;                                       // s_blk buffer of the current unit
-    bool issued = false;                              // its first stages are in flight
-
-    float o[D / 8][4];
-    float m_run, l_run;
-    while (u < units) {
-        const Unit nx = describe(un);
-        // the next unit's block ids: in flight while this unit streams
-        int nb_bad = 0, nb_id = -1;
-        if (nx.live && tid < nx.nblk) nb_id = load_id(nx, tid, nb_bad);
-
-        const int s = cu.s, part = cu.part, L = cu.L, tok0 = cu.tok0, kvh = cu.kvh;
-        const int h0 = cu.h0, nh = cu.nh, nchunk = cu.nchunk, nparts = cu.nparts;
-        int timed_out = 0;
-        if (cu.live) {
-            // ---- per-warp TMA ring over the partition's 16-row stages --------
-            const int my_n = nchunk > warp ? (nchunk - warp + kDecWarps - 1) / kDecWarps : 0;
-            if (!issued && lane == 0) {
-                fence_proxy_async_smem();
-                for (int k = 0; k < min(NS, my_n); ++k) issue(s_blk[cb], kvh, k, kt);
-            }
-
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-            m_run = -INFINITY;
-            l_run = 0.f;
-
-            for (int k = 0; k < my_n; ++k) {
-                const uint32_t st = (kt + k) % NS;
-                const bool ok = mbar_wait(bar0 + st * 8, ((kt + k) / NS) & 1u, err);
-                if (!__all_sync(0xffffffffu, ok)) {     // leave together: shuffles follow
-                    timed_out = 1;
-                    break;
-                }
-                const int pos0 = tok0 + (warp + k * kDecWarps) * kRows;
-                const int valid = min(kRows, L - pos0);
-                const uint32_t kbase = ring + st * Cfg::kStageBytes;
-                const uint32_t vbase = kbase + Cfg::kSlabBytes;
-                float sc[2][4];
-
-                if constexpr (FP8) {
-                    if (valid < kRows) {
-                        // tokens past the sequence may hold anything (even NaN): zero
-                        // their codes in every row of the transposed V tile
-                        uint8_t* vt = smem + (vbase - smem_u32(smem));
-                        for (int row = lane; row < D; row += 32) {
-                            uint4 w = *reinterpret_cast<uint4*>(vt + row * 16);
-                            uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int keep = min(4, max(0, valid - 4 * e));     // bytes kept
-                                ww[e] &= keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
-                            }
-                            *reinterpret_cast<uint4*>(vt + row * 16) = w;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    // S = Q K^T.  Column j of n-tile nt is token 4*(j/2) + 2*nt + j%2,
-                    // which leaves P in the token order the V fragments use below.
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-                        const int i = lane & 7;
-                        const int r = 4 * (i >> 1) + 2 * nt + (i & 1);
-#pragma unroll
-                        for (int kq = 0; kq < D / 64; ++kq) {
-                            const int cidx = kq * 4 + (lane >> 3);
-                            const int sw = D == 128 ? (cidx ^ (r & 7)) : (cidx ^ ((r >> 1) & 3));
-                            uint32_t w[4];
-                            ldsm_x4(kbase + r * D + (sw << 4), w[0], w[1], w[2], w[3]);
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) {
-                                const int kk = kq * 4 + jj;
-                                const uint32_t a[4] = {qa[kk][0], 0u, qa[kk][1], 0u};
-                                uint32_t b0, b1;
-                                e4m3x4_to_h2x2(w[jj], b0, b1);
-                                MmaOp<T>::run(sc[nt], a, b0, b1);
-                            }
-                        }
-                    }
-                } else {
-                    if (valid < kRows) {
-                        // rows past the sequence may hold anything (even NaN): zero them in
-                        // V so that 0 * row stays 0 inside the MMA
-                        uint8_t* vgen = smem + (vbase - smem_u32(smem));
-                        const int nbytes = (kRows - valid) * 128;
-                        for (int hx = 0; hx < kHalves; ++hx)
-                            for (int off = lane * 16; off < nbytes; off += 32 * 16)
-                                *reinterpret_cast<uint4*>(vgen + hx * kHalfTile + valid * 128 + off) =
-                                    make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    // S = Q K^T for the 16 rows
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-                        for (int kc = 0; kc < D / 16; kc += 2) {
-                            const int r = nt * 8 + (lane & 7);
-                            const int chunk = kc * 2 + (lane >> 3);
-                            const uint32_t addr = kbase + (chunk >> 3) * kHalfTile + r * 128 +
-                                                  (((chunk & 7) ^ (r & 7)) << 4);
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4(addr, b0, b1, b2, b3);
-                            const uint32_t a0[4] = {qa[kc][0], 0u, qa[kc][1], 0u};
-                            const uint32_t a1[4] = {qa[kc + 1][0], 0u, qa[kc + 1][1], 0u};
-                            MmaOp<T>::run(sc[nt], a0, b0, b1);
-                            MmaOp<T>::run(sc[nt], a1, b2, b3);
-                        }
-                    }
-                }
-
-                // online softmax on row g (log2 domain)
-                float mx = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int p = pos0 + (FP8 ? 4 * t4 + 2 * nt + e : nt * 8 + 2 * t4 + e);
-                        const float z = p < L ? sc[nt][e] * scale_log2 : -INFINITY;
-                        sc[nt][e] = z;
-                        mx = fmaxf(mx, z);
-                    }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run, mx);
-                // rescale only when some row's running max moved (warp-uniform
-                // branch; after the first stages the max rarely moves).  The first
-                // stage has m_run = -inf: alpha = 0 clears the (zero) state.
-                if (__any_sync(0xffffffffu, m_new != m_run)) {
-                    const float alpha = fast_exp2(m_run - m_new);
-                    l_run *= alpha;
-#pragma unroll
-                    for (int i = 0; i < D / 8; ++i) {
-                        o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha; o[i][3] *= alpha;
-                    }
-                }
-                m_run = m_new;
-                float psum = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float p = fast_exp2(sc[nt][e] - m_new);
-                        sc[nt][e] = p;
-                        psum += p;
-                    }
-                l_run += psum;
-
-                // O += P V, P as hi (rows 0-7) + lo (rows 8-15)
-                uint32_t pa[4];
-                split_pair<T>(sc[0][0], sc[0][1], pa[0], pa[1]);
-                split_pair<T>(sc[1][0], sc[1][1], pa[2], pa[3]);
-                if constexpr (FP8) {
-                    // transposed V tile: row d holds tokens 0..15; a fragment word is
-                    // tokens 4*t4 .. 4*t4+3 of row d, the k order P is in
-#pragma unroll
-                    for (int nd = 0; nd < D / 8; nd += 4) {
-                        const int d_row = (nd + (lane >> 3)) * 8 + (lane & 7);
-                        uint32_t w[4];
-                        ldsm_x4(vbase + d_row * 16, w[0], w[1], w[2], w[3]);
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                        {
-                            uint32_t b0, b1;
-                            e4m3x4_to_h2x2(w[jj], b0, b1);
-                            MmaOp<T>::run(o[nd + jj], pa, b0, b1);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int nt = 0; nt < D / 8; nt += 2) {
-                        const int mi = lane >> 3;
-                        const int r = (mi & 1) * 8 + (lane & 7);
-                        const int chunk = nt + (mi >> 1);
-                        const uint32_t addr = vbase + (chunk >> 3) * kHalfTile + r * 128 +
-                                              (((chunk & 7) ^ (r & 7)) << 4);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(addr, b0, b1, b2, b3);
-                        MmaOp<T>::run(o[nt], pa, b0, b1);
-                        MmaOp<T>::run(o[nt + 1], pa, b2, b3);
-                    }
-                }
-
-                __syncwarp();
-                if (lane == 0 && k + NS < my_n) {
-                    fence_proxy_async_smem();
-                    issue(s_blk[cb], kvh, k + NS, kt);
-                }
-            }
-            kt += my_n;
-            // ---- this warp's share of the combine
-            l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-            l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-            if constexpr (Cfg::kSepRed) {
-#pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt) {
-                    float* dst = red_o + (warp * 8 + g) * D + nt * 8 + 2 * t4;
-                    dst[0] = o[nt][0] + o[nt][2];
-                    dst[1] = o[nt][1] + o[nt][3];
-                }
-                if (t4 == 0) {
-                    red_m[warp * 8 + g] = m_run;
-                    red_l[warp * 8 + g] = l_run;
-                }
-            }
-        }
-        if (nx.live && tid < nx.nblk) s_blk[cb ^ 1][tid] = nb_id;
-        // every ring is idle and (separate buffer) the partials are written
-        const int flags = __syncthreads_or(timed_out | (nb_bad << 1));
-        if (flags & 1) return;
-        if (tid == 0) s_next = static_cast<long long>(gridDim.x) + atomicAdd(ticket, 1u);
-        const bool next_live = nx.live && !(flags & 2);
-        if (cu.live) {
-            if constexpr (!Cfg::kSepRed) {
-                // the combine buffer aliases the rings: written after the barrier
-#pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt) {
-                    float* dst = red_o + (warp * 8 + g) * D + nt * 8 + 2 * t4;
-                    dst[0] = o[nt][0] + o[nt][2];
-                    dst[1] = o[nt][1] + o[nt][3];
-                }
-                if (t4 == 0) {
-                    red_m[warp * 8 + g] = m_run;
-                    red_l[warp * 8 + g] = l_run;
-                }
-                fence_proxy_async_smem();   // these generic writes precede later TMA writes here
-                __syncthreads();
-            }
-        }
-        issued = false;
-        if constexpr (Cfg::kSepRed) {
-            if (next_live && lane == 0) {
-                fence_proxy_async_smem();
-                const int n1 = my_stages(nx);
-                for (int k = 0; k < min(NS, n1); ++k) issue(s_blk[cb ^ 1], nx.kvh, k, kt);
-            }
-            issued = true;
-        }
-        if (next_live) load_q(nx);                    // its latency overlaps the combine
-        if (cu.live) {
-            for (int idx = tid; idx < nh * D; idx += kDecWarps * 32) {
-                const int hh = idx / D, dd = idx - hh * D;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
-                float lsum = 0.f, acc = 0.f;
-#pragma unroll
-                for (int w = 0; w < kDecWarps; ++w) {
-                    const float f = exp2f(red_m[w * 8 + hh] - M);
-                    lsum += f * red_l[w * 8 + hh];
-                    acc += f * red_o[(w * 8 + hh) * D + dd];
-                }
-                acc *= v_scale;                                    // 1 unless the pool is FP8
-                const int64_t sh = static_cast<int64_t>(s) * n_q + h0 + hh;
-                if (nparts == 1) {
-                    store_any(out, sh * D + dd, acc / lsum, out_dtype);
-                } else {
-                    const int64_t w_idx = sh * max_parts + part;
-                    ws_acc[w_idx * D + dd] = acc;
-                    if (dd == 0) {
-                        ws_ml[2 * w_idx] = M;
-                        ws_ml[2 * w_idx + 1] = lsum;
-                    }
-                }
-            }
-        }
-        // the combine's reads are done before any warp writes partials (or, when
-        // they alias the rings, TMA data) again; s_next is visible to all
-        __syncthreads();
-        u = un;
-        un = s_next;
-        cu = nx;
-        cu.live = next_live;
-        cb ^= 1;
-    }
-}
 
 // CUDA-core path: one warp per (partition, query head, sequence).
 template <typename T, int DPL>
@@ -689,14 +88,15 @@ template <int DPL>
 __global__ void __launch_bounds__(128)
 decode_reduce_kernel(void* __restrict__ out, pa_dtype out_dtype,
                      const int32_t* __restrict__ context_lens, const float* __restrict__ ws_ml,
-                     const float* __restrict__ ws_acc, int num_seqs, int n_q, int part_tokens,
-                     int max_parts)
+                     const float* __restrict__ ws_acc, int num_seqs, int n_q, int nq,
+                     int part_tokens, int max_parts)
 {
     constexpr int D = DPL * 32;
     const int lane = threadIdx.x & 31;
+    // one warp per output row ((sequence, query) x head)
     const int64_t sh = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-    if (sh >= static_cast<int64_t>(num_seqs) * n_q) return;
-    const int s = static_cast<int>(sh / n_q);
+    if (sh >= static_cast<int64_t>(num_seqs) * nq * n_q) return;
+    const int s = static_cast<int>(sh / (static_cast<int64_t>(nq) * n_q));
     const int L = __ldg(context_lens + s);
     const int J = min((L + part_tokens - 1) / part_tokens, max_parts);
     if (J <= 1) return;
@@ -723,71 +123,6 @@ decode_reduce_kernel(void* __restrict__ out, pa_dtype out_dtype,
 
 // ------------------------------------------------------------------ launch
 
-static int sm_count()
-{
-    static std::mutex mu;
-    static int cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-        cache[dev] = n;
-    }
-    return cache[dev];
-}
-
-template <typename T, typename QT, int D, int BS, bool FP8>
-static cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
-{
-    // FP8 runs 3 CTAs per SM (registers capped at 168 by the launch bounds):
-    // Llama-3-8B batch 0.273 -> 0.231 ms against 2 CTAs with 24 KB rings.
-    constexpr int NS = decode_stages<T, D, FP8>();
-    using Cfg = DecodeCfg<T, D, NS, FP8>;
-    auto kern = decode_mma_kernel<T, QT, D, BS, NS, FP8>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int per_sm = 1;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Cfg::kDynBytes);
-        if (attr_err == cudaSuccess &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecWarps * 32,
-                                                          Cfg::kDynBytes) != cudaSuccess)
-            per_sm = 1;
-        if (per_sm < 1) per_sm = 1;
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap kmap, vmap;
-    const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
-    if constexpr (FP8) {
-        // K: rows of D codes, 128- (D 128) or 64-byte (D 64) swizzle; V: the
-        // transposed slabs viewed as rows of block_size codes, one row per
-        // (block, head, head-dim element)
-        const uint64_t vrows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * D;
-        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, D, kRows, D) != PA_OK ||
-            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, BS, vrows, kRows, D, 0) != PA_OK)
-            return cudaErrorInvalidValue;
-    } else {
-        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK ||
-            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK)
-            return cudaErrorInvalidValue;
-    }
-    const int group = a.n_q / a.cache.n_kv_heads;
-    const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.max_parts * a.cache.n_kv_heads *
-                          ((group + 7) / 8);
-    const int64_t resident = static_cast<int64_t>(sm_count()) * per_sm;
-    const unsigned grid = static_cast<unsigned>(upper < resident ? upper : resident);
-    kern<<<grid, kDecWarps * 32, Cfg::kDynBytes, s>>>(
-        kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
-        a.context_lens, a.num_seqs, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
-        FP8 ? scale_log2 * a.cache.k_scale : scale_log2, FP8 ? a.cache.v_scale : 1.f, a.ws_ml,
-        a.ws_acc, a.part_tokens, a.max_parts, a.ticket, a.err);
-    return cudaGetLastError();
-}
-
 template <typename T, int DPL>
 static cudaError_t run_simt(const DecodeArgs& a, cudaStream_t s, float scale_log2)
 {
@@ -813,36 +148,14 @@ static cudaError_t run_simt_dt(const DecodeArgs& a, cudaStream_t s, float sl2)
     }
 }
 
-template <typename T>
-static cudaError_t run_mma_dt(const DecodeArgs& a, cudaStream_t s, float sl2)
-{
-    const int D = a.cache.head_dim, BS = a.cache.block_size;
-    if (D == 64 && BS == 16) return run_mma<T, T, 64, 16, false>(a, s, sl2);
-    if (D == 64 && BS == 32) return run_mma<T, T, 64, 32, false>(a, s, sl2);
-    if (D == 128 && BS == 16) return run_mma<T, T, 128, 16, false>(a, s, sl2);
-    if (D == 128 && BS == 32) return run_mma<T, T, 128, 32, false>(a, s, sl2);
-    return run_simt_dt<T>(a, s, sl2);
-}
-
-template <typename QT>
-static cudaError_t run_fp8_qt(const DecodeArgs& a, cudaStream_t s, float sl2)
-{
-    const int D = a.cache.head_dim, BS = a.cache.block_size;
-    if (D == 64 && BS == 16) return run_mma<__half, QT, 64, 16, true>(a, s, sl2);
-    if (D == 64 && BS == 32) return run_mma<__half, QT, 64, 32, true>(a, s, sl2);
-    if (D == 128 && BS == 16) return run_mma<__half, QT, 128, 16, true>(a, s, sl2);
-    if (D == 128 && BS == 32) return run_mma<__half, QT, 128, 32, true>(a, s, sl2);
-    return cudaErrorInvalidValue;
-}
-
 static cudaError_t run_reduce(const DecodeArgs& a, cudaStream_t s)
 {
-    const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.n_q;
+    const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.q_per_seq * a.n_q;
     const unsigned grid = static_cast<unsigned>((pairs + 3) / 4);
 #define PA_REDUCE(DPL)                                                                          \
     decode_reduce_kernel<DPL><<<grid, 128, 0, s>>>(a.out, a.out_dtype, a.context_lens, a.ws_ml, \
-                                                   a.ws_acc, a.num_seqs, a.n_q, a.part_tokens,  \
-                                                   a.max_parts)
+                                                   a.ws_acc, a.num_seqs, a.n_q, a.q_per_seq,    \
+                                                   a.part_tokens, a.max_parts)
     switch (a.cache.head_dim) {
         case 32: PA_REDUCE(1); break;
         case 64: PA_REDUCE(2); break;
@@ -866,14 +179,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
     profile_events(&ev0, &ev1);
     if (ev0) cudaEventRecord(ev0, s);
     cudaError_t e;
-    switch (a.cache.dtype) {
-        case PA_BF16: e = run_mma_dt<__nv_bfloat16>(a, s, sl2); break;
-        case PA_F16: e = run_mma_dt<__half>(a, s, sl2); break;
-        case PA_FP8_E4M3:
-            e = a.cache.act_dtype == PA_BF16 ? run_fp8_qt<__nv_bfloat16>(a, s, sl2)
-                                             : run_fp8_qt<__half>(a, s, sl2);
-            break;
-        default: e = run_simt_dt<float>(a, s, sl2); break;
+    if (a.q_per_seq > 1) {
+        e = launch_decode_mq(a, s, sl2);
+    } else {
+        e = run_mma_any<false>(a, s, sl2);
+        if (e == cudaErrorNotSupported) {        // fp32 pools, other head dims
+            switch (a.cache.dtype) {
+                case PA_BF16: e = run_simt_dt<__nv_bfloat16>(a, s, sl2); break;
+                case PA_F16: e = run_simt_dt<__half>(a, s, sl2); break;
+                default: e = run_simt_dt<float>(a, s, sl2); break;
+            }
+        }
     }
     if (ev1) cudaEventRecord(ev1, s);
     if (e != cudaSuccess) return e;

@@ -11,7 +11,7 @@ namespace pa {
 
 // Tokens per decode partition for a launch: every partition of a sequence but
 // its last covers exactly this many tokens (a multiple of the block size).
-int decode_partition_tokens(int num_seqs, int n_kv_heads, int block_size, int max_context_len);
+int decode_partition_tokens(int64_t seq_groups, int block_size, int max_context_len);
 
 // Records a host-side failure message for pa_last_error_message().
 pa_status fail(pa_status st, const char* fmt, ...);
@@ -48,14 +48,17 @@ struct DecodeArgs {
     const void* k_cache; const void* v_cache; pa_cache_desc cache;
     const int32_t* block_tables; int max_blocks;
     const int32_t* context_lens; int num_seqs; int n_q; float scale;
-    float* ws_ml;      // [B][n_q][J][2] (m, l) or null
-    float* ws_acc;     // [B][n_q][J][d] or null
+    int q_per_seq;     // query rows per sequence (1 for decode; k+1 to verify k drafts)
+    float* ws_ml;      // [B][q_per_seq][n_q][J][2] (m, l) or null
+    float* ws_acc;     // [B][q_per_seq][n_q][J][d] or null
     int part_tokens;   // tokens per partition
     int max_parts;     // J: partitions of the longest possible sequence
     unsigned* ticket;  // work counter in the workspace's control area
     unsigned* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// attention kernel of a call with q_per_seq > 1 (decode_verify.cu)
+cudaError_t launch_decode_mq(const DecodeArgs& a, cudaStream_t s, float scale_log2);
 
 struct PrefillArgs {
     void* out; pa_dtype out_dtype; const void* q;
