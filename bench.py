@@ -38,11 +38,15 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic of the main decode kernel on this workload, per launch
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
-# source is byte-identical to what was profiled (sha256 of csrc/decode.cu).
+# sources are byte-identical to what was profiled (sha256 of DECODE_SOURCES).
 NCU_TRAFFIC = {
-    # ncu --set full on a 64-sequence case of the same shapes, scaled by unique
-    # K/V bytes to the 256-sequence workload (profiles/decode_mma_llama3-8b-bf16_b64_full.md)
-    ("llama3-8b-bf16", 256, "1de313c840c68565"): 2402456678,
+    # one-pass ncu captures (--metrics dram__bytes_read.sum,dram__bytes_write.sum,
+    # full-size workload, 4th launch); profiles/decode_dram_full_size.md
+    ("llama3-8b-bf16", 256, "1a7a48696a67773b"): 2372081152 + 13510144,
+    ("llama3-8b-fp8", 256, "1a7a48696a67773b"): 1188188416 + 12797952,
+    ("llama3-8b-bf16-verify4", 256, "1a7a48696a67773b"): 2386673408 + 45770240,
+    ("opt13b-fp16", 128, "1a7a48696a67773b"): 5371655680 + 8446464,
+    ("mixed-llama3-8b-bf16", 192, "1a7a48696a67773b"): 1446115840 + 9917952,
 }
 
 
@@ -68,9 +72,16 @@ def _peaks_tensor():
         return 1700.0, "bf16 sustained (fallback)"
 
 
-def _src_hash(name: str) -> str:
-    with open(os.path.join(ROOT, "paged_kv_cache_25_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+# the decode kernel's sources: traffic figures hold only while these are unchanged
+DECODE_SOURCES = ("decode_mma.cuh", "decode.cu", "decode_verify.cu", "pa_device.cuh")
+
+
+def _src_hash(names) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_25_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def _cores() -> int:
@@ -172,7 +183,10 @@ def oracle_sample(wl_name: str, n_seqs: int | None, target_s: float, seed_offset
                 v = oracle.dequantize_fp8(oracle.quantize_fp8(v, wl.kv_scale), wl.kv_scale)
             ks.append(k); vs.append(v)
         t0 = time.perf_counter()
-        oracle.decode(q_all[seqs], ks, vs, wl.scale, threads=threads)
+        if wl.q_per_seq == 1:
+            oracle.decode(q_all[seqs], ks, vs, wl.scale, threads=threads)
+        else:   # several query rows per sequence: chunks of q_per_seq rows
+            oracle.prefill([q_all[s] for s in seqs], ks, vs, wl.scale, threads=threads)
         return time.perf_counter() - t0
 
     if n_seqs is None:
@@ -369,7 +383,7 @@ def run_ours(args, rank, world, local_rank):
     # algorithmic bytes of the main decode kernel per launch: the unique K/V
     # bytes plus q, the output/partials are < 0.5% and not counted
     achieved = kv_unique / (dec_ms * 1e-3) / 1e9
-    src = _src_hash("decode.cu")
+    src = _src_hash(DECODE_SOURCES)
     tr = NCU_TRAFFIC.get((wl.name, B, src))
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -381,14 +395,15 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": wl.name, "batch": B, "n_q_heads": wl.n_q_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "num_blocks": st.num_blocks,
-                   "prefill_requests": st.R, "parallelism": f"replicas x{world}",
+                   "prefill_requests": st.R, "q_per_seq": wl.q_per_seq,
+                   "parallelism": f"replicas x{world}",
                    "l2": (f"inputs larger than L2 ({pool_bytes / 1e9:.2f} GB pool, "
                           f"{kv_unique / 1e9:.2f} GB of K/V read per step); no flush"
                           if flush is None else
                           f"L2 flushed before every timed step (a {2 * l2_bytes >> 20} MiB write, "
                           "outside the step's events); the pool "
                           f"({pool_bytes / 1e6:.0f} MB) would fit in L2")},
-        "decode_tokens_per_s": world * B / (ms_step * 1e-3),
+        "decode_tokens_per_s": world * B * wl.q_per_seq / (ms_step * 1e-3),
         "steps_per_s": 1e3 / ms_step,
         "pct_of_hbm_peak": 100.0 * value / world / peak,
         "kv_bytes_unique_per_step": kv_unique, "kv_bytes_logical_per_step": kv_logical,

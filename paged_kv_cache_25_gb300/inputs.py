@@ -21,6 +21,9 @@ Workloads (the KV shapes are single transformer layers):
                      bs 16, bf16, pool 1.5x the blocks needed.
 * ``opt13b-fp16``    128 sequences, every length 2048, 40/40 heads, d 128, bs 16,
                      fp16, values N(0, 0.5) (standard deviation 0.5).
+* ``llama3-8b-bf16-verify4``  the Llama-3-8B decode batch (same lengths and K/V)
+                     where each sequence brings 4 query rows (3 drafted tokens to
+                     verify plus one), the last 4 rows of its context.
 * ``llama3-8b-fp8``  the Llama-3-8B decode batch (same draws) stored in an FP8
                      E4M3 pool with K and V scale 1/64.
 * ``mixed-llama3-8b-bf16``  one continuous-batching step on Llama-3-8B shapes with
@@ -71,6 +74,7 @@ class Workload:
     prefill_ctx_range: tuple = (0, 0)
     cache_dtype: torch.dtype | None = None   # pool dtype when it differs (FP8 pools)
     kv_scale: float = 1.0                     # FP8 pools: per-tensor scale of K and V
+    q_per_seq: int = 1                        # query rows per decode sequence (k+1 to verify k drafts)
 
     @property
     def pool_dtype(self) -> torch.dtype:
@@ -104,6 +108,10 @@ WORKLOADS = {
                                lens_kind="uniform", lens_args=(512, 4096)),
     "opt13b-fp16": Workload("opt13b-fp16", 1004, 128, 40, 40, 128, 16, torch.float16, std=0.5,
                             lens_kind="const", lens_args=(2048,)),
+    # the Llama-3-8B decode batch verifying 3 drafted tokens per sequence (4 query rows)
+    "llama3-8b-bf16-verify4": Workload("llama3-8b-bf16-verify4", 1003, 256, 32, 8, 128, 16,
+                                       torch.bfloat16, lens_kind="uniform",
+                                       lens_args=(512, 4096), q_per_seq=4),
     # the Llama-3-8B decode batch with an FP8 E4M3 pool (K and V scale 1/64)
     "llama3-8b-fp8": Workload("llama3-8b-fp8", 1003, 256, 32, 8, 128, 16, torch.bfloat16,
                               lens_kind="uniform", lens_args=(512, 4096),
@@ -197,8 +205,11 @@ class Draws:
 
     # ---- tensors ----------------------------------------------------------
     def q(self) -> torch.Tensor:
+        """[B][n_q][d], or [B][q_per_seq][n_q][d] when a sequence has several rows."""
         wl = self.wl
-        return _normal(_rng(self.seed, "q"), (wl.batch, wl.n_q_heads, wl.head_dim), wl.std, wl.dtype)
+        shape = ((wl.batch, wl.n_q_heads, wl.head_dim) if wl.q_per_seq == 1 else
+                 (wl.batch, wl.q_per_seq, wl.n_q_heads, wl.head_dim))
+        return _normal(_rng(self.seed, "q"), shape, wl.std, wl.dtype)
 
     def prefix_kv(self):
         wl = self.wl

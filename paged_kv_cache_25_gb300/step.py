@@ -8,8 +8,9 @@ pa_reshape_and_cache exactly as a serving loop would have appended it.
 
 One step (the timed hot path): append the new tokens' K/V
 (pa_reshape_and_cache), decode one token for every decode sequence
-(pa_decode, split-K plus reduce), and run the chunked-prefill requests, if
-any (pa_prefill_chunk).  All three run in the library's CUDA kernels.
+(pa_decode, split-K plus reduce; pa_decode_verify when a sequence brings
+several query rows), and run the chunked-prefill requests, if any
+(pa_prefill_chunk).  All of it runs in the library's CUDA kernels.
 """
 from __future__ import annotations
 
@@ -81,16 +82,16 @@ class PagedStep:
         self._prefill_context(upload_chunk_tokens)
 
         # ---- per-step inputs ------------------------------------------------
-        B = wl.batch
+        B, nq = wl.batch, wl.q_per_seq
         self.q = dr.q().to(dev)
-        new_k = torch.empty((B, n_kv, d), dtype=wl.dtype)
-        new_v = torch.empty((B, n_kv, d), dtype=wl.dtype)
+        new_k = torch.empty((B * nq, n_kv, d), dtype=wl.dtype)
+        new_v = torch.empty((B * nq, n_kv, d), dtype=wl.dtype)
         prefix = dr.prefix_kv() if self.prefix else None
-        for s in range(B):   # the newest row of every decode sequence
+        for s in range(B):   # the newest row(s) of every decode sequence
             k, v = dr.seq_kv(s, int(self.lens[s]), bool(self.sharers[s]), prefix)
-            new_k[s], new_v[s] = k[-1], v[-1]
-        seq = np.arange(B, dtype=np.int32)
-        pos = (self.lens - 1).astype(np.int32)
+            new_k[s * nq:(s + 1) * nq], new_v[s * nq:(s + 1) * nq] = k[-nq:], v[-nq:]
+        seq = np.repeat(np.arange(B, dtype=np.int32), nq)
+        pos = (self.lens[:, None] - nq + np.arange(nq)[None, :]).reshape(-1).astype(np.int32)
         slots = pa.pa_slot_mapping(self.tables, bs, seq, pos)
         ks, vs, ss = [new_k], [new_v], [slots]
         self.p_q = []
@@ -107,8 +108,9 @@ class PagedStep:
         self.block_tables = torch.from_numpy(self.tables).to(dev)
         self.context_lens = torch.from_numpy(self.lens.astype(np.int32)).to(dev)
         od = out_dtype or wl.dtype
-        self.out = torch.empty((B, wl.n_q_heads, d), dtype=od, device=dev)
-        ws = pa.pa_decode_workspace_size(B, wl.n_q_heads, n_kv, d, bs, self.max_blocks * bs)
+        self.out = torch.empty(tuple(self.q.shape), dtype=od, device=dev)
+        ws = pa.pa_decode_verify_workspace_size(B, nq, wl.n_q_heads, n_kv, d, bs,
+                                                self.max_blocks * bs)
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev) if ws else None
         if self.R:
             self.p_q_dev = torch.cat(self.p_q).to(dev).contiguous()
@@ -158,7 +160,7 @@ class PagedStep:
                 if first_sharer_done:
                     start = self.prefix           # the shared blocks are written once
                 first_sharer_done = True
-            add(k, v, self.tables, s, start, L - 1)
+            add(k, v, self.tables, s, start, L - wl.q_per_seq)
         for r in range(self.R):
             k, v = dr.prefill_kv(r, int(self.p_lens[r]))
             add(k, v, self.p_tables, r, 0, int(self.p_ctx[r]))
@@ -178,9 +180,10 @@ class PagedStep:
         around the chunked-prefill kernel."""
         wl = self.wl
         self._write(self.new_k, self.new_v, self.new_slots, stream=stream)
-        pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
-                     self.context_lens, wl.scale, wl.block_size, self.workspace, stream=stream,
-                     **self.kv_scales)
+        decode = pa.pa_decode if wl.q_per_seq == 1 else pa.pa_decode_verify
+        decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+               self.context_lens, wl.scale, wl.block_size, self.workspace, stream=stream,
+               **self.kv_scales)
         if self.R:
             if prefill_events is not None:
                 prefill_events[0].record(stream or torch.cuda.current_stream())

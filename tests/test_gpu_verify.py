@@ -174,3 +174,22 @@ def test_verify_host_checks():
                             wl.scale, wl.block_size,
                             torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
     assert pa.pa_get_device_error() == 0
+
+
+def test_verify_full_size_workload_sampled():
+    """The Llama-3-8B batch with 4 query rows per sequence, as the bench runs
+    it (cache write of the 4 new rows, then the multi-query decode)."""
+    from paged_kv_cache_25_gb300.step import PagedStep
+    wl = inputs.get("llama3-8b-bf16-verify4")
+    st = PagedStep(wl, out_dtype=torch.float32)
+    st.step()
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    order = np.argsort(st.lens)
+    seqs = sorted({int(order[0]), int(order[-1]), 3, 77, 150, 201})
+    dr = st.draws
+    q = dr.q()
+    ks, vs = zip(*(dr.seq_kv(s, int(st.lens[s])) for s in seqs))
+    ref = np.stack(oracle.prefill([q[s] for s in seqs], list(ks), list(vs), wl.scale))
+    assert max_err(st.out[seqs], ref) <= TOL[wl.dtype]
+    assert torch.isfinite(st.out).all()
