@@ -6,22 +6,24 @@
 // read through the request's block table; the chunk's own K/V are already in
 // the pool.
 //
-// CTA = (128 M rows, KV head, request).  The M rows are (position, head) pairs
-// of one GQA group, position-major, so one pass over the keys serves all the
-// query heads that share the KV head.  Keys go in tiles of 64.
+// CTA = (256 M rows, KV head, request) as two 128-row tiles A and B that share
+// one stream of K/V.  The M rows are (position, head) pairs of one GQA group,
+// position-major, so one pass over the keys serves all the query heads that
+// share the KV head.  Keys go in tiles of 64.
 //   warps 8, 9: TMA producers: 16-row K (warp 8) and V (warp 9) slabs of each
 //             64-key tile into their own 3-stage rings (128-byte swizzle), one
 //             block-table lookup per block;
-//   warp 10 : one thread issues the MMAs: S = Q K^T (M 128, N 64, K = d) into a
-//             double-buffered TMEM tile, then O += P V (M 128, N = d, K 64)
-//             into TMEM, signalling completion with tcgen05.commit;
-//   warps 0-7: two threads per M row (each half of the keys and of O): read S
-//             from TMEM, causal mask on absolute positions, online softmax in
-//             base 2 with lazy rescaling (O in TMEM
+//   warp 10 : one thread issues the MMAs: S_t = Q_t K^T (M 128, N 64, K = d)
+//             into double-buffered TMEM tiles, then O_t += P_t V (M 128, N = d,
+//             K 64) into TMEM, for t = A, B, signalling with tcgen05.commit;
+//   warps 0-3 (tile A), 4-7 (tile B): one thread per M row reads its 64
+//             scores from TMEM, applies the causal mask on absolute positions,
+//             runs the online softmax in base 2 with lazy rescaling (O in TMEM
 //             is rescaled only when the running max grows by more than 2^8),
-//             P written to shared memory as hi + lo bf16/fp16 halves so that P V
-//             keeps ~16 bits of P, final O / l written to global memory.
-// All waits are bounded; the kernel never traps.
+//             and writes P to shared memory as hi + lo bf16/fp16 halves so that
+//             P V keeps ~16 bits of P; at the end O / l goes to global memory.
+// While one tile's rows run their softmax the tensor cores work on the other
+// tile's products.  All waits are bounded; the kernel never traps.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -32,26 +34,31 @@
 
 namespace pa {
 
-constexpr int kTcRows = 128;      // M rows per CTA
+constexpr int kTcRows = 128;      // M rows per tile
+constexpr int kTcTiles = 2;       // tiles per CTA (A, B)
 constexpr int kTcKeys = 64;       // keys per tile
 constexpr int kTcStages = 3;      // K/V ring depth
-constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxWarps = 4 * kTcTiles;
 constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1, kMmaWarp = kSoftmaxWarps + 2;
 constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;   // softmax, K producer, V producer, MMA
-constexpr uint32_t kTmemCols = 256;   // S0 [0,64) S1 [64,128) O [128, 128 + d)
+constexpr uint32_t kTmemCols = 512;   // S_A[2] [0,128) S_B[2] [128,256) O_A, O_B from 256
 
 template <typename T, int D>
 struct PfLayout {
     static constexpr int kHalves = D / 64;
-    static constexpr uint32_t kQBytes = kTcRows * D * 2;          // Q tile
+    static constexpr uint32_t kQBytes = kTcRows * D * 2;          // one Q tile
     static constexpr uint32_t kPBytes = kTcRows * kTcKeys * 2;    // one of P hi / P lo
-    static constexpr uint32_t kKBytes = kTcKeys * D * 2;          // K (or V) of one tile
-    static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffP = kOffQ + kQBytes;     // 2 buffers x (P hi, P lo)
-    static constexpr uint32_t kPBuf = 2 * kPBytes;
-    static constexpr uint32_t kOffK = kOffP + 2 * kPBuf;        // K ring
+    static constexpr uint32_t kKBytes = kTcKeys * D * 2;          // K (or V) of one key tile
+    static constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
+    static constexpr uint32_t kOffK = kOffQ + kTcTiles * kQBytes; // K ring
     static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
-    static constexpr uint32_t kDynBytes = kOffV + kTcStages * kKBytes + 1024;
+    static constexpr uint32_t kOffP = kOffV + kTcStages * kKBytes;   // (P hi, P lo) of A, of B
+    static constexpr uint32_t kPTile = 2 * kPBytes;
+    static constexpr uint32_t kDynBytes = kOffP + kTcTiles * kPTile + 1024;
+    static constexpr uint32_t kTmemS = 0;                         // + t * 128 + buffer * 64
+    static constexpr uint32_t kTmemO = 256;                       // + t * D
+    static_assert(kDynBytes <= 232448, "shared memory per CTA");
+    static_assert(kTmemO + kTcTiles * D <= kTmemCols, "tensor memory columns");
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -99,29 +106,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     constexpr uint32_t kIdescPV = idesc_f16(kBf16, false, true, kTcRows, D);
     static_assert(BS % 16 == 0 && kTcKeys % BS == 0, "block size must divide the key tile");
 
-    // tiles with more keys first: the last position tiles are the heaviest
-    const int tile = gridDim.x - 1 - blockIdx.x;
+    // blocks with more keys first: the last position blocks are the heaviest
+    const int blk = gridDim.x - 1 - blockIdx.x;
     const int kvh = blockIdx.y, r = blockIdx.z;
     const int qs = __ldg(q_start + r);
     const int C = __ldg(q_start + r + 1) - qs;
     const int L = __ldg(context_lens + r);
     const int rows_total = C * group;
-    const int row0 = tile * kTcRows;
+    const int row0 = blk * (kTcTiles * kTcRows);
     if (row0 >= rows_total) return;
     if (C > L || C < 0) {
         if (threadIdx.x == 0) set_error(err, PA_ERR_OUT_OF_RANGE);
         return;
     }
     const int ctx0 = L - C;
-    const int last_row = min(rows_total, row0 + kTcRows) - 1;
-    const int n_tiles = (ctx0 + last_row / group) / kTcKeys + 1;
+    // key tiles each tile's rows need (0: the tile has no rows)
+    int n_t[kTcTiles];
+#pragma unroll
+    for (int t = 0; t < kTcTiles; ++t) {
+        const int first = row0 + t * kTcRows;
+        const int last = min(rows_total, first + kTcRows) - 1;
+        n_t[t] = first < rows_total ? (ctx0 + last / group) / kTcKeys + 1 : 0;
+    }
+    const int n_tiles = max(n_t[0], n_t[1]);
 
     __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages];
     __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
-    __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_ready;
-    __shared__ __align__(8) uint64_t pair_bar[4];
-    __shared__ float xmax[2][2][kTcRows];
-    __shared__ float xl[2][kTcRows];
+    __shared__ __align__(8) uint64_t s_full[kTcTiles][2], s_free[kTcTiles][2];
+    __shared__ __align__(8) uint64_t p_full[kTcTiles], pv_done[kTcTiles], q_ready;
     __shared__ uint32_t s_tmem;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -136,15 +148,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mbar_init(smem_u32(&v_full[i]), 1);
             mbar_init(smem_u32(&v_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&s_empty[i]), kSoftmaxWarps);
+        for (int t = 0; t < kTcTiles; ++t) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(smem_u32(&s_full[t][i]), 1);
+                mbar_init(smem_u32(&s_free[t][i]), 4);
+            }
+            mbar_init(smem_u32(&p_full[t]), 4);
+            mbar_init(smem_u32(&pv_done[t]), 1);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&pair_bar[i]), 2);
-        mbar_init(smem_u32(&p_full[0]), kSoftmaxWarps);
-        mbar_init(smem_u32(&p_full[1]), kSoftmaxWarps);
-        mbar_init(smem_u32(&pv_done[0]), 1);
-        mbar_init(smem_u32(&pv_done[1]), 1);
         mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
     }
     if (warp == kMmaWarp) {
@@ -159,9 +170,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 
     if (warp == kKWarp || warp == kVWarp) {
         // ------------------------------------------------ TMA producers
-        // K and V have separate rings: K of tile j is released as soon as
-        // S_j = Q K_j^T is done, V of tile j once P_j V_j is done, so each ring
-        // can run kTcStages tiles ahead of its consumer.
+        // K and V have separate rings: K of key tile j is released as soon as
+        // both S_t = Q_t K_j^T are done, V of tile j once both P_t V_j are, so
+        // each ring runs up to kTcStages tiles ahead of its consumer.
         if (lane == 0) {
             const bool is_k = warp == kKWarp;
             const CUtensorMap* map = is_k ? &kmap : &vmap;
@@ -200,84 +211,101 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // ------------------------------------------------ MMA issuer
         // Descriptors are built once; each MMA only adds a constant to the
         // start-address field (16-byte units; every operand lies below 256 KB).
+        // Order per key tile j: S_A(j), S_B(j), then O_A += P_A(j-1) V, O_B +=
+        // P_B(j-1) V, so the scores of tile j are ready while the rows run the
+        // softmax of tile j - 1.
         if (lane == 0) {
             const uint64_t dq = sdesc_sw128(sbase + Ly::kOffQ, 16, 1024);
             const uint64_t dk = sdesc_sw128(sbase + Ly::kOffK, 16, 1024);
             const uint64_t dp = sdesc_sw128(sbase + Ly::kOffP, 16, 1024);
             const uint64_t dv = sdesc_sw128(sbase + Ly::kOffV, kTcKeys * 128, 1024);
             constexpr uint32_t kQHalf = (kTcRows * 128) >> 4, kKHalf = (kTcKeys * 128) >> 4;
-            constexpr uint32_t kKStage = Ly::kKBytes >> 4, kPBufU = Ly::kPBuf >> 4;
-            constexpr uint32_t kPLo = Ly::kPBytes >> 4;
-            const uint32_t d_o = tmem + 128;
+            constexpr uint32_t kKStage = Ly::kKBytes >> 4, kQTile = Ly::kQBytes >> 4;
+            constexpr uint32_t kPTileU = Ly::kPTile >> 4, kPLo = Ly::kPBytes >> 4;
             bool ok = mbar_wait(smem_u32(&q_ready), 0, err);
             tc_fence_after();
             for (int j = 0; ok && j <= n_tiles; ++j) {
                 if (j < n_tiles) {
                     const int st = j % kTcStages, sb = j & 1;
                     if (!mbar_wait(smem_u32(&k_full[st]), (j / kTcStages) & 1, err)) break;
-                    if (j >= 2 && !mbar_wait(smem_u32(&s_empty[sb]), ((j >> 1) - 1) & 1, err)) break;
-                    tc_fence_after();
                     const uint64_t dks = dk + st * kKStage;
-                    const uint32_t d_s = tmem + sb * kTcKeys;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
-                        const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
-                        umma_f16(d_s, dq + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
+                    for (int t = 0; t < kTcTiles; ++t) {
+                        if (j >= n_t[t]) continue;
+                        if (j >= 2 && !mbar_wait(smem_u32(&s_free[t][sb]), ((j >> 1) - 1) & 1, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_s = tmem + Ly::kTmemS + t * 128 + sb * kTcKeys;
+                        const uint64_t dqt = dq + t * kQTile;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
+                            const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
+                            umma_f16(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(smem_u32(&s_full[t][sb]));
                     }
-                    umma_commit(smem_u32(&s_full[sb]));
+                    if (!ok) break;
                     umma_commit(smem_u32(&k_empty[st]));
                 }
                 if (j >= 1) {
                     const int jp = j - 1, stp = jp % kTcStages;
-                    if (!mbar_wait(smem_u32(&p_full[jp & 1]), (jp >> 1) & 1, err)) break;
                     if (!mbar_wait(smem_u32(&v_full[stp]), (jp / kTcStages) & 1, err)) break;
-                    tc_fence_after();
-                    const uint64_t dps = dp + (jp & 1) * kPBufU;
                     const uint64_t dvs = dv + stp * kKStage;
 #pragma unroll
-                    for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-                        umma_f16(d_o, dps + ks * 2, dvs + ks * (2048 >> 4), kIdescPV,
-                                 (jp > 0 || ks > 0) ? 1u : 0u);
-                        umma_f16(d_o, dps + kPLo + ks * 2, dvs + ks * (2048 >> 4), kIdescPV, 1u);
+                    for (int t = 0; t < kTcTiles; ++t) {
+                        if (jp >= n_t[t]) continue;
+                        if (!mbar_wait(smem_u32(&p_full[t]), jp & 1, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_o = tmem + Ly::kTmemO + t * D;
+                        const uint64_t dps = dp + t * kPTileU;
+#pragma unroll
+                        for (int ks = 0; ks < kTcKeys / 16; ++ks) {
+                            umma_f16(d_o, dps + ks * 2, dvs + ks * (2048 >> 4), kIdescPV,
+                                     (jp > 0 || ks > 0) ? 1u : 0u);
+                            umma_f16(d_o, dps + kPLo + ks * 2, dvs + ks * (2048 >> 4), kIdescPV, 1u);
+                        }
+                        umma_commit(smem_u32(&pv_done[t]));
                     }
-                    umma_commit(smem_u32(&pv_done[jp & 1]));
+                    if (!ok) break;
                     umma_commit(smem_u32(&v_empty[stp]));
                 }
             }
         }
     } else {
         // ------------------------------------------------ softmax warps 0-7
-        // Warp w reads TMEM lanes 32*(w % 4) .. +31 (its M rows) and handles
-        // half (w / 4) of every tile's 64 keys and of the O columns; the two
-        // warps sharing rows swap their partial row maxima through shared
-        // memory and a two-arrival mbarrier (a bounded wait).
-        const int quarter = warp & 3, half = warp >> 2;
-        const int rr = quarter * 32 + lane;                 // M row = TMEM lane
-        const int grow = row0 + rr;
+        // Warp w serves tile t = w / 4 and reads TMEM lanes 32*(w % 4) .. +31:
+        // thread = M row, all 64 keys of every key tile, all D columns of O.
+        const int t = warp >> 2, quarter = warp & 3;
+        const int rr = quarter * 32 + lane;                 // M row in the tile = TMEM lane
+        const int grow = row0 + t * kTcRows + rr;
         const bool valid = grow < rows_total;
         const int pos_local = valid ? grow / group : 0;
         const int head = kvh * group + (valid ? grow - (grow / group) * group : 0);
         const int p_abs = valid ? ctx0 + pos_local : L - 1;   // padding rows see every key
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t xbar = smem_u32(&pair_bar[quarter]);
-        constexpr int kHalfKeys = kTcKeys / 2;
-        constexpr int kHalfD = D / 2;
+        const uint32_t s_col = Ly::kTmemS + t * 128, o_col = Ly::kTmemO + t * D;
+        const int nt = n_t[t];
 
-        // Q row -> shared memory, 128-byte swizzled rows (each warp of the pair
-        // writes half of the row).  A negative scale is applied as -Q and
-        // |scale| (an exact sign flip), so the raw-score max is the scaled max.
+        // Q row -> shared memory, 128-byte swizzled rows.  A negative scale is
+        // applied as -Q and |scale| (an exact sign flip), so the raw-score max
+        // is the scaled max.
         const uint32_t qsign = scale_log2 < 0.f ? 0x80008000u : 0u;
         scale_log2 = fabsf(scale_log2);
         {
             const uint4* qp = reinterpret_cast<const uint4*>(
                 q + (static_cast<int64_t>(qs + pos_local) * n_q + head) * D);
+            const uint32_t qbase = sbase + Ly::kOffQ + t * Ly::kQBytes;
 #pragma unroll
-            for (int cc = 0; cc < D / 16; ++cc) {
-                const int c = half * (D / 16) + cc;
+            for (int c = 0; c < D / 8; ++c) {
                 uint4 v = valid ? __ldg(qp + c) : make_uint4(0, 0, 0, 0);
                 v.x ^= qsign; v.y ^= qsign; v.z ^= qsign; v.w ^= qsign;
-                const uint32_t addr = sbase + Ly::kOffQ + (c >> 3) * (kTcRows * 128) + rr * 128 +
+                const uint32_t addr = qbase + (c >> 3) * (kTcRows * 128) + rr * 128 +
                                       (((c & 7) ^ (rr & 7)) << 4);
                 st_shared_v4(addr, v.x, v.y, v.z, v.w);
             }
@@ -287,53 +315,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
 
         // smallest query position of this warp's rows (rows are position-major)
-        const int wrow = row0 + quarter * 32;
+        const int wrow = row0 + t * kTcRows + quarter * 32;
         const int warp_min_pos = wrow < rows_total ? ctx0 + wrow / group : L - 1;
+        const uint32_t pbase = sbase + Ly::kOffP + t * Ly::kPTile;
         float m_raw = -INFINITY, l = 0.f;
         bool broken = false;
-        int j = 0;
-        for (; j < n_tiles; ++j) {
+        for (int j = 0; j < nt; ++j) {
             const int sb = j & 1;
-            const bool ok = mbar_wait(smem_u32(&s_full[sb]), (j >> 1) & 1, err);
+            const bool ok = mbar_wait(smem_u32(&s_full[t][sb]), (j >> 1) & 1, err);
             if (!__all_sync(0xffffffffu, ok)) {
                 broken = true;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[kHalfKeys];
-            tmem_ld32(lane_addr + sb * kTcKeys + half * kHalfKeys, sr);
+            uint32_t sr[kTcKeys];
+            tmem_ld32(lane_addr + s_col + sb * kTcKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(lane_addr + s_col + sb * kTcKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
+            if (lane == 0) mbar_arrive(smem_u32(&s_free[t][sb]));
 
             // scores stay raw (unscaled) until the exponent: the max is taken on
             // raw values and p = 2^(s*c - m*c) is one FFMA and one EX2
-            const int key0 = j * kTcKeys + half * kHalfKeys;
-            const bool full_tile = key0 + kHalfKeys - 1 <= warp_min_pos;
+            const int key0 = j * kTcKeys;
+            const bool full_tile = key0 + kTcKeys - 1 <= warp_min_pos;
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (full_tile) {
 #pragma unroll
-                for (int i = 0; i < kHalfKeys; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+                for (int i = 0; i < kTcKeys; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
             } else {
 #pragma unroll
-                for (int i = 0; i < kHalfKeys; ++i) {
+                for (int i = 0; i < kTcKeys; ++i) {
                     const float z = (key0 + i <= p_abs) ? __uint_as_float(sr[i]) : -INFINITY;
                     sr[i] = __float_as_uint(z);
                     m4[i & 3] = fmaxf(m4[i & 3], z);
                 }
             }
-            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            // swap partial maxima with the partner warp (exchange number j)
-            xmax[j & 1][half][rr] = mx;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xbar);
-            const bool okx = mbar_wait(xbar, j & 1, err);
-            if (!__all_sync(0xffffffffu, okx)) {
-                broken = true;
-                break;
-            }
-            mx = fmaxf(mx, xmax[j & 1][half ^ 1][rr]);
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 
             // lazy: move the reference max only when the first tile sets it or
             // the max grew by more than 2^8 (written so that scale 0 stays finite)
@@ -346,69 +365,73 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 l *= fac;
             }
             const float neg_mc = -m_raw * scale_log2;
-            uint32_t ph[kHalfKeys / 2], pl[kHalfKeys / 2];
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-            if (full_tile) {
-#pragma unroll
-                for (int i = 0; i < kHalfKeys / 2; ++i) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
-                    s4[i & 3] += p0 + p1;
-                    split_trunc<T>(p0, p1, ph[i], pl[i]);
-                }
-            } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
-#pragma unroll
-                for (int i = 0; i < kHalfKeys / 2; ++i) {
-                    const float s0 = __uint_as_float(sr[2 * i]), s1 = __uint_as_float(sr[2 * i + 1]);
-                    const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(fmaf(s0, scale_log2, neg_mc));
-                    const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(fmaf(s1, scale_log2, neg_mc));
-                    s4[i & 3] += p0 + p1;
-                    split_trunc<T>(p0, p1, ph[i], pl[i]);
-                }
-            }
-            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
 
-            // O is rescaled only when the reference max moved: that needs the
-            // previous P V finished (no MMA writes O while it is rescaled)
-            if (j >= 1 && __any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
-                const bool ok2 = mbar_wait(smem_u32(&pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, err);
+            // P (j) overwrites P (j - 1): that P V must be done.  The same wait
+            // lets O be rescaled (no MMA writes O meanwhile).
+            if (j >= 1) {
+                const bool ok2 = mbar_wait(smem_u32(&pv_done[t]), (j - 1) & 1, err);
                 if (!__all_sync(0xffffffffu, ok2)) {
                     broken = true;
                     break;
                 }
                 tc_fence_after();
+                if (__any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
 #pragma unroll
-                for (int c0 = 0; c0 < kHalfD; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_addr + 128 + half * kHalfD + c0, o);
-                    tmem_ld_wait();
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_addr + o_col + c0, o);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
-                    tmem_st32(lane_addr + 128 + half * kHalfD + c0, o);
-                }
-                tmem_st_wait();
-            }
-            // P buffer (j & 1) is free once the P V of tile j - 2 is done
-            if (j >= 2) {
-                const bool ok3 = mbar_wait(smem_u32(&pv_done[j & 1]), ((j - 2) >> 1) & 1, err);
-                if (!__all_sync(0xffffffffu, ok3)) {
-                    broken = true;
-                    break;
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
+                        tmem_st32(lane_addr + o_col + c0, o);
+                    }
+                    tmem_st_wait();
                 }
             }
-            const uint32_t pbuf = sbase + Ly::kOffP + (j & 1) * Ly::kPBuf;
+
+            // P in two halves of 32 keys: exponent, row sum, hi/lo split, store
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int cc = 0; cc < kHalfKeys / 8; ++cc) {
-                const int c = half * (kHalfKeys / 8) + cc;
-                const uint32_t sw = ((c ^ (rr & 7)) << 4);
-                st_shared_v4(pbuf + rr * 128 + sw, ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2], ph[4 * cc + 3]);
-                st_shared_v4(pbuf + Ly::kPBytes + rr * 128 + sw, pl[4 * cc], pl[4 * cc + 1], pl[4 * cc + 2], pl[4 * cc + 3]);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t ph[16], pl[16];
+                if (full_tile) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int k = hf * 32 + 2 * i;
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[k]), scale_log2, neg_mc));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[k + 1]), scale_log2, neg_mc));
+                        s4[i & 3] += p0 + p1;
+                        split_trunc<T>(p0, p1, ph[i], pl[i]);
+                    }
+                } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int k = hf * 32 + 2 * i;
+                        const float s0 = __uint_as_float(sr[k]), s1 = __uint_as_float(sr[k + 1]);
+                        const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(fmaf(s0, scale_log2, neg_mc));
+                        const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(fmaf(s1, scale_log2, neg_mc));
+                        s4[i & 3] += p0 + p1;
+                        split_trunc<T>(p0, p1, ph[i], pl[i]);
+                    }
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = hf * 4 + cc;                 // 16-byte chunk of the 128-byte row
+                    const uint32_t sw = ((c ^ (rr & 7)) << 4);
+                    st_shared_v4(pbase + rr * 128 + sw, ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2],
+                                 ph[4 * cc + 3]);
+                    st_shared_v4(pbase + Ly::kPBytes + rr * 128 + sw, pl[4 * cc], pl[4 * cc + 1],
+                                 pl[4 * cc + 2], pl[4 * cc + 3]);
+                }
             }
+            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+
             const int tkey0 = j * kTcKeys;
             if (tkey0 + kTcKeys > L) {
-                // keys at or past L (only in the request's last tile) may hold
+                // keys at or past L (only in the request's last key tile) may hold
                 // anything, even NaN: zero those V rows so P = 0 keeps them out,
-                // after the tile's V has landed
+                // after the tile's V has landed.  Both tiles' rows may do this for
+                // the same key tile; they write the same zeros.
                 const bool okv = mbar_wait(smem_u32(&v_full[j % kTcStages]), (j / kTcStages) & 1, err);
                 if (!__all_sync(0xffffffffu, okv)) {
                     broken = true;
@@ -417,7 +440,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const int valid_rows = max(0, L - tkey0);
                 const int per_half = (kTcKeys - valid_rows) * 8;      // 16-byte pieces
                 const uint32_t vb = sbase + Ly::kOffV + (j % kTcStages) * Ly::kKBytes;
-                for (int i = tid; i < per_half * Ly::kHalves; i += 8 * 32) {
+                for (int i = quarter * 32 + lane; i < per_half * Ly::kHalves; i += 4 * 32) {
                     const int hx = i / per_half;
                     const int rem = i - hx * per_half;
                     st_shared_v4(vb + hx * (kTcKeys * 128) + valid_rows * 128 + rem * 16, 0, 0, 0, 0);
@@ -426,29 +449,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full[j & 1]));
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
         }
 
         // ------------------------------------------------ epilogue: O / l
-        if (!broken) {
-            xl[half][rr] = l;                   // swap partial sums (exchange n_tiles)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xbar);
-            const bool okx = mbar_wait(xbar, n_tiles & 1, err);
-            const bool ok = mbar_wait(smem_u32(&pv_done[(n_tiles - 1) & 1]), ((n_tiles - 1) >> 1) & 1, err);
-            if (__all_sync(0xffffffffu, ok && okx)) {
+        if (!broken && nt > 0) {
+            const bool ok = mbar_wait(smem_u32(&pv_done[t]), (nt - 1) & 1, err);
+            if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                const float inv = 1.f / (l + xl[half ^ 1][rr]);
+                const float inv = 1.f / l;
                 const int64_t obase = (static_cast<int64_t>(qs + pos_local) * n_q + head) * D;
 #pragma unroll
-                for (int c0 = 0; c0 < kHalfD; c0 += 32) {
+                for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
-                    tmem_ld32(lane_addr + 128 + half * kHalfD + c0, o);
+                    tmem_ld32(lane_addr + o_col + c0, o);
                     tmem_ld_wait();
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv;
-                    if (valid) store_row<T>(out, obase, half * kHalfD + c0, v, 32, out_dtype);
+                    if (valid) store_row<T>(out, obase, c0, v, 32, out_dtype);
                 }
             }
         }
@@ -478,7 +497,8 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
         encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK)
         return cudaErrorInvalidValue;
     const int group = a.n_q / a.cache.n_kv_heads;
-    const int64_t tiles = (static_cast<int64_t>(a.max_q) * group + kTcRows - 1) / kTcRows;
+    const int64_t tiles = (static_cast<int64_t>(a.max_q) * group + kTcTiles * kTcRows - 1) /
+                          (kTcTiles * kTcRows);
     dim3 grid(static_cast<unsigned>(tiles), a.cache.n_kv_heads, a.num_reqs);
     kern<<<grid, kTcThreads, Ly::kDynBytes, s>>>(
         kmap, vmap, a.out, a.out_dtype, static_cast<const T*>(a.q), a.block_tables, a.max_blocks,
