@@ -20,8 +20,10 @@
 //             scores from TMEM, applies the causal mask on absolute positions,
 //             runs the online softmax in base 2 with lazy rescaling (O in TMEM
 //             is rescaled only when the running max grows by more than 2^8),
-//             and writes P to shared memory as hi + lo bf16/fp16 halves so that
-//             P V keeps ~16 bits of P; at the end O / l goes to global memory.
+//             and writes P back over its scores in TMEM as hi + lo bf16/fp16
+//             halves (P V keeps ~16 bits of P); the P V MMA takes P straight
+//             from TMEM, so P costs no shared-memory traffic.  At the end O / l
+//             goes to global memory.
 // While one tile's rows run their softmax the tensor cores work on the other
 // tile's products.  All waits are bounded; the kernel never traps.
 #include "pa_device.cuh"
@@ -47,15 +49,14 @@ template <typename T, int D>
 struct PfLayout {
     static constexpr int kHalves = D / 64;
     static constexpr uint32_t kQBytes = kTcRows * D * 2;          // one Q tile
-    static constexpr uint32_t kPBytes = kTcRows * kTcKeys * 2;    // one of P hi / P lo
     static constexpr uint32_t kKBytes = kTcKeys * D * 2;          // K (or V) of one key tile
     static constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
     static constexpr uint32_t kOffK = kOffQ + kTcTiles * kQBytes; // K ring
     static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
-    static constexpr uint32_t kOffP = kOffV + kTcStages * kKBytes;   // (P hi, P lo) of A, of B
-    static constexpr uint32_t kPTile = 2 * kPBytes;
-    static constexpr uint32_t kDynBytes = kOffP + kTcTiles * kPTile + 1024;
-    static constexpr uint32_t kTmemS = 0;                         // + t * 128 + buffer * 64
+    static constexpr uint32_t kDynBytes = kOffV + kTcStages * kKBytes + 1024;
+    // S_t[b] at t * 128 + b * 64; P_t(j) overwrites S_t[j & 1]: hi in its first
+    // 32 columns, lo in the next 32 (two 16-bit values per column)
+    static constexpr uint32_t kTmemS = 0;
     static constexpr uint32_t kTmemO = 256;                       // + t * D
     static_assert(kDynBytes <= 232448, "shared memory per CTA");
     static_assert(kTmemO + kTcTiles * D <= kTmemCols, "tensor memory columns");
@@ -133,7 +134,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages];
     __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
     __shared__ __align__(8) uint64_t s_full[kTcTiles][2], s_free[kTcTiles][2];
-    __shared__ __align__(8) uint64_t p_full[kTcTiles], pv_done[kTcTiles], q_ready;
+    // one p_full / pv_done pair per S/P buffer: a waiter is never two phases
+    // behind (P of tile j + 2 needs the scores of j + 2, issued after P V of j)
+    __shared__ __align__(8) uint64_t p_full[kTcTiles][2], pv_done[kTcTiles][2], q_ready;
     __shared__ uint32_t s_tmem;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -153,8 +156,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 mbar_init(smem_u32(&s_full[t][i]), 1);
                 mbar_init(smem_u32(&s_free[t][i]), 4);
             }
-            mbar_init(smem_u32(&p_full[t]), 4);
-            mbar_init(smem_u32(&pv_done[t]), 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(smem_u32(&p_full[t][i]), 4);
+                mbar_init(smem_u32(&pv_done[t][i]), 1);
+            }
         }
         mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
     }
@@ -217,11 +222,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (lane == 0) {
             const uint64_t dq = sdesc_sw128(sbase + Ly::kOffQ, 16, 1024);
             const uint64_t dk = sdesc_sw128(sbase + Ly::kOffK, 16, 1024);
-            const uint64_t dp = sdesc_sw128(sbase + Ly::kOffP, 16, 1024);
             const uint64_t dv = sdesc_sw128(sbase + Ly::kOffV, kTcKeys * 128, 1024);
             constexpr uint32_t kQHalf = (kTcRows * 128) >> 4, kKHalf = (kTcKeys * 128) >> 4;
             constexpr uint32_t kKStage = Ly::kKBytes >> 4, kQTile = Ly::kQBytes >> 4;
-            constexpr uint32_t kPTileU = Ly::kPTile >> 4, kPLo = Ly::kPBytes >> 4;
             bool ok = mbar_wait(smem_u32(&q_ready), 0, err);
             tc_fence_after();
             for (int j = 0; ok && j <= n_tiles; ++j) {
@@ -257,20 +260,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
                     for (int t = 0; t < kTcTiles; ++t) {
                         if (jp >= n_t[t]) continue;
-                        if (!mbar_wait(smem_u32(&p_full[t]), jp & 1, err)) {
+                        if (!mbar_wait(smem_u32(&p_full[t][jp & 1]), (jp >> 1) & 1, err)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint32_t d_o = tmem + Ly::kTmemO + t * D;
-                        const uint64_t dps = dp + t * kPTileU;
+                        const uint32_t a_p = tmem + Ly::kTmemS + t * 128 + (jp & 1) * kTcKeys;
 #pragma unroll
-                        for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-                            umma_f16(d_o, dps + ks * 2, dvs + ks * (2048 >> 4), kIdescPV,
-                                     (jp > 0 || ks > 0) ? 1u : 0u);
-                            umma_f16(d_o, dps + kPLo + ks * 2, dvs + ks * (2048 >> 4), kIdescPV, 1u);
+                        for (int ks = 0; ks < kTcKeys / 16; ++ks) {   // 16 keys = 8 columns
+                            umma_f16_ts(d_o, a_p + ks * 8, dvs + ks * (2048 >> 4), kIdescPV,
+                                        (jp > 0 || ks > 0) ? 1u : 0u);
+                            umma_f16_ts(d_o, a_p + 32 + ks * 8, dvs + ks * (2048 >> 4), kIdescPV, 1u);
                         }
-                        umma_commit(smem_u32(&pv_done[t]));
+                        umma_commit(smem_u32(&pv_done[t][jp & 1]));
                     }
                     if (!ok) break;
                     umma_commit(smem_u32(&v_empty[stp]));
@@ -317,7 +320,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // smallest query position of this warp's rows (rows are position-major)
         const int wrow = row0 + t * kTcRows + quarter * 32;
         const int warp_min_pos = wrow < rows_total ? ctx0 + wrow / group : L - 1;
-        const uint32_t pbase = sbase + Ly::kOffP + t * Ly::kPTile;
         float m_raw = -INFINITY, l = 0.f;
         bool broken = false;
         for (int j = 0; j < nt; ++j) {
@@ -366,16 +368,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             const float neg_mc = -m_raw * scale_log2;
 
-            // P (j) overwrites P (j - 1): that P V must be done.  The same wait
-            // lets O be rescaled (no MMA writes O meanwhile).
-            if (j >= 1) {
-                const bool ok2 = mbar_wait(smem_u32(&pv_done[t]), (j - 1) & 1, err);
+            // O is rescaled only when the reference max moved: that needs the
+            // previous P V done (no MMA writes O meanwhile)
+            if (j >= 1 && __any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
+                const bool ok2 = mbar_wait(smem_u32(&pv_done[t][(j - 1) & 1]), ((j - 1) >> 1) & 1, err);
                 if (!__all_sync(0xffffffffu, ok2)) {
                     broken = true;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
+                {
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t o[32];
@@ -389,42 +391,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
             }
 
-            // P in two halves of 32 keys: exponent, row sum, hi/lo split, store
+            // P: exponent, row sum, hi/lo split, written over S_t[sb] in TMEM
+            // (the scores were read above; their MMA ordered before this P V)
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t ph[kTcKeys / 2], pl[kTcKeys / 2];
+            if (full_tile) {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t ph[16], pl[16];
-                if (full_tile) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int k = hf * 32 + 2 * i;
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[k]), scale_log2, neg_mc));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[k + 1]), scale_log2, neg_mc));
-                        s4[i & 3] += p0 + p1;
-                        split_trunc<T>(p0, p1, ph[i], pl[i]);
-                    }
-                } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int k = hf * 32 + 2 * i;
-                        const float s0 = __uint_as_float(sr[k]), s1 = __uint_as_float(sr[k + 1]);
-                        const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(fmaf(s0, scale_log2, neg_mc));
-                        const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(fmaf(s1, scale_log2, neg_mc));
-                        s4[i & 3] += p0 + p1;
-                        split_trunc<T>(p0, p1, ph[i], pl[i]);
-                    }
+                for (int i = 0; i < kTcKeys / 2; ++i) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
+                    s4[i & 3] += p0 + p1;
+                    split_trunc<T>(p0, p1, ph[i], pl[i]);
                 }
+            } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = hf * 4 + cc;                 // 16-byte chunk of the 128-byte row
-                    const uint32_t sw = ((c ^ (rr & 7)) << 4);
-                    st_shared_v4(pbase + rr * 128 + sw, ph[4 * cc], ph[4 * cc + 1], ph[4 * cc + 2],
-                                 ph[4 * cc + 3]);
-                    st_shared_v4(pbase + Ly::kPBytes + rr * 128 + sw, pl[4 * cc], pl[4 * cc + 1],
-                                 pl[4 * cc + 2], pl[4 * cc + 3]);
+                for (int i = 0; i < kTcKeys / 2; ++i) {
+                    const float s0 = __uint_as_float(sr[2 * i]), s1 = __uint_as_float(sr[2 * i + 1]);
+                    const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(fmaf(s0, scale_log2, neg_mc));
+                    const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(fmaf(s1, scale_log2, neg_mc));
+                    s4[i & 3] += p0 + p1;
+                    split_trunc<T>(p0, p1, ph[i], pl[i]);
                 }
             }
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            tmem_st32(lane_addr + s_col + sb * kTcKeys, ph);
+            tmem_st32(lane_addr + s_col + sb * kTcKeys + 32, pl);
+            tmem_st_wait();
 
             const int tkey0 = j * kTcKeys;
             if (tkey0 + kTcKeys > L) {
@@ -446,15 +438,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     st_shared_v4(vb + hx * (kTcKeys * 128) + valid_rows * 128 + rem * 16, 0, 0, 0, 0);
                 }
             }
-            fence_proxy_async_smem();
+            if (tkey0 + kTcKeys > L) fence_proxy_async_smem();   // the zeroed V rows
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[t][sb]));
         }
 
         // ------------------------------------------------ epilogue: O / l
         if (!broken && nt > 0) {
-            const bool ok = mbar_wait(smem_u32(&pv_done[t]), (nt - 1) & 1, err);
+            const bool ok = mbar_wait(smem_u32(&pv_done[t][(nt - 1) & 1]), ((nt - 1) >> 1) & 1, err);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float inv = 1.f / l;
