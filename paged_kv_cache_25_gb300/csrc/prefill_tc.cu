@@ -9,23 +9,22 @@
 // CTA = (256 M rows, KV head, request) as two 128-row tiles A and B that share
 // one stream of K/V.  The M rows are (position, head) pairs of one GQA group,
 // position-major, so one pass over the keys serves all the query heads that
-// share the KV head.  Keys go in tiles of 64.
+// share the KV head.  Keys go in tiles of 128.
 //   warps 8, 9: TMA producers: 16-row K (warp 8) and V (warp 9) slabs of each
-//             64-key tile into their own 3-stage rings (128-byte swizzle), one
+//             128-key tile into their own 2-stage rings (128-byte swizzle), one
 //             block-table lookup per block;
-//   warp 10 : one thread issues the MMAs: S_t = Q_t K^T (M 128, N 64, K = d)
-//             into double-buffered TMEM tiles, then O_t += P_t V (M 128, N = d,
-//             K 64) into TMEM, for t = A, B, signalling with tcgen05.commit;
-//   warps 0-3 (tile A), 4-7 (tile B): one thread per M row reads its 64
+//   warp 10 : one thread issues the MMAs: S_t = Q_t K^T (M 128, N 128, K = d)
+//             into TMEM, O_t += P_t V (M 128, N = d, K 128) into TMEM, in the
+//             order P_A(j) V, S_A(j+1), P_B(j) V, S_B(j+1): while one tile's rows
+//             run their softmax the tensor cores work on the other tile;
+//   warps 0-3 (tile A), 4-7 (tile B): one thread per M row reads its 128
 //             scores from TMEM, applies the causal mask on absolute positions,
 //             runs the online softmax in base 2 with lazy rescaling (O in TMEM
 //             is rescaled only when the running max grows by more than 2^8),
 //             and writes P back over its scores in TMEM as hi + lo bf16/fp16
 //             halves (P V keeps ~16 bits of P); the P V MMA takes P straight
-//             from TMEM, so P costs no shared-memory traffic.  At the end O / l
-//             goes to global memory.
-// While one tile's rows run their softmax the tensor cores work on the other
-// tile's products.  All waits are bounded; the kernel never traps.
+//             from TMEM.  At the end O / l goes to global memory.
+// All waits are bounded; the kernel never traps.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -38,12 +37,12 @@ namespace pa {
 
 constexpr int kTcRows = 128;      // M rows per tile
 constexpr int kTcTiles = 2;       // tiles per CTA (A, B)
-constexpr int kTcKeys = 64;       // keys per tile
-constexpr int kTcStages = 3;      // K/V ring depth
+constexpr int kTcKeys = 128;      // keys per key tile
+constexpr int kTcStages = 2;      // K/V ring depth
 constexpr int kSoftmaxWarps = 4 * kTcTiles;
 constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1, kMmaWarp = kSoftmaxWarps + 2;
 constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;   // softmax, K producer, V producer, MMA
-constexpr uint32_t kTmemCols = 512;   // S_A[2] [0,128) S_B[2] [128,256) O_A, O_B from 256
+constexpr uint32_t kTmemCols = 512;   // S/P_A [0,128) S/P_B [128,256) O_A, O_B from 256
 
 template <typename T, int D>
 struct PfLayout {
@@ -54,8 +53,8 @@ struct PfLayout {
     static constexpr uint32_t kOffK = kOffQ + kTcTiles * kQBytes; // K ring
     static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
     static constexpr uint32_t kDynBytes = kOffV + kTcStages * kKBytes + 1024;
-    // S_t[b] at t * 128 + b * 64; P_t(j) overwrites S_t[j & 1]: hi in its first
-    // 32 columns, lo in the next 32 (two 16-bit values per column)
+    // S_t at t * 128; P_t overwrites it, keys 64h .. 64h+63 as hi in columns
+    // 64h .. 64h+31 and lo in 64h+32 .. 64h+63 (two 16-bit values per column)
     static constexpr uint32_t kTmemS = 0;
     static constexpr uint32_t kTmemO = 256;                       // + t * D
     static_assert(kDynBytes <= 232448, "shared memory per CTA");
@@ -121,7 +120,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         return;
     }
     const int ctx0 = L - C;
-    // key tiles each tile's rows need (0: the tile has no rows)
+    // key tiles each tile's rows need (0: the tile has no rows); n_t[0] <= n_t[1]
     int n_t[kTcTiles];
 #pragma unroll
     for (int t = 0; t < kTcTiles; ++t) {
@@ -131,12 +130,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     }
     const int n_tiles = max(n_t[0], n_t[1]);
 
+    // Every barrier below is waited on in completion order and its waiter is
+    // never two phases behind: S_t(j + 1) is issued after P_t(j) V, which
+    // waits for P_t(j), which needs S_t(j).
     __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages];
     __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
-    __shared__ __align__(8) uint64_t s_full[kTcTiles][2], s_free[kTcTiles][2];
-    // one p_full / pv_done pair per S/P buffer: a waiter is never two phases
-    // behind (P of tile j + 2 needs the scores of j + 2, issued after P V of j)
-    __shared__ __align__(8) uint64_t p_full[kTcTiles][2], pv_done[kTcTiles][2], q_ready;
+    __shared__ __align__(8) uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles], q_ready;
     __shared__ uint32_t s_tmem;
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -152,14 +151,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mbar_init(smem_u32(&v_empty[i]), 1);
         }
         for (int t = 0; t < kTcTiles; ++t) {
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(smem_u32(&s_full[t][i]), 1);
-                mbar_init(smem_u32(&s_free[t][i]), 4);
-            }
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(smem_u32(&p_full[t][i]), 4);
-                mbar_init(smem_u32(&pv_done[t][i]), 1);
-            }
+            mbar_init(smem_u32(&s_full[t]), 1);
+            mbar_init(smem_u32(&p_full[t]), 4);
+            mbar_init(smem_u32(&pv_done[t]), 1);
         }
         mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
     }
@@ -175,9 +169,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 
     if (warp == kKWarp || warp == kVWarp) {
         // ------------------------------------------------ TMA producers
-        // K and V have separate rings: K of key tile j is released as soon as
-        // both S_t = Q_t K_j^T are done, V of tile j once both P_t V_j are, so
-        // each ring runs up to kTcStages tiles ahead of its consumer.
+        // K and V have separate rings: K of key tile j is released once both
+        // S_t(j) are done, V of tile j once both P_t(j) V are.
         if (lane == 0) {
             const bool is_k = warp == kKWarp;
             const CUtensorMap* map = is_k ? &kmap : &vmap;
@@ -216,74 +209,74 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // ------------------------------------------------ MMA issuer
         // Descriptors are built once; each MMA only adds a constant to the
         // start-address field (16-byte units; every operand lies below 256 KB).
-        // Order per key tile j: S_A(j), S_B(j), then O_A += P_A(j-1) V, O_B +=
-        // P_B(j-1) V, so the scores of tile j are ready while the rows run the
-        // softmax of tile j - 1.
         if (lane == 0) {
             const uint64_t dq = sdesc_sw128(sbase + Ly::kOffQ, 16, 1024);
             const uint64_t dk = sdesc_sw128(sbase + Ly::kOffK, 16, 1024);
             const uint64_t dv = sdesc_sw128(sbase + Ly::kOffV, kTcKeys * 128, 1024);
             constexpr uint32_t kQHalf = (kTcRows * 128) >> 4, kKHalf = (kTcKeys * 128) >> 4;
             constexpr uint32_t kKStage = Ly::kKBytes >> 4, kQTile = Ly::kQBytes >> 4;
-            bool ok = mbar_wait(smem_u32(&q_ready), 0, err);
+            // S_t(j) = Q_t K_j^T; the K stage is released after the last tile's
+            auto issue_qk = [&](int t, int j) {
+                const int st = j % kTcStages;
+                const uint64_t dks = dk + st * kKStage;
+                const uint32_t d_s = tmem + Ly::kTmemS + t * 128;
+                const uint64_t dqt = dq + t * kQTile;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
+                    const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
+                    umma_f16(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(smem_u32(&s_full[t]));
+            };
+            // O_t += P_t(j) V_j, P from TMEM (hi and lo halves of each 16 keys)
+            auto issue_pv = [&](int t, int j) {
+                const int st = j % kTcStages;
+                const uint64_t dvs = dv + st * kKStage;
+                const uint32_t d_o = tmem + Ly::kTmemO + t * D;
+                const uint32_t a_p = tmem + Ly::kTmemS + t * 128;
+#pragma unroll
+                for (int ks = 0; ks < kTcKeys / 16; ++ks) {
+                    const uint32_t col = (ks >> 2) * 64 + (ks & 3) * 8;   // 16 keys = 8 columns
+                    umma_f16_ts(d_o, a_p + col, dvs + ks * (2048 >> 4), kIdescPV,
+                                (j > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16_ts(d_o, a_p + col + 32, dvs + ks * (2048 >> 4), kIdescPV, 1u);
+                }
+                umma_commit(smem_u32(&pv_done[t]));
+            };
+            bool ok = mbar_wait(smem_u32(&q_ready), 0, err) &&
+                      mbar_wait(smem_u32(&k_full[0]), 0, err);
             tc_fence_after();
-            for (int j = 0; ok && j <= n_tiles; ++j) {
-                if (j < n_tiles) {
-                    const int st = j % kTcStages, sb = j & 1;
-                    if (!mbar_wait(smem_u32(&k_full[st]), (j / kTcStages) & 1, err)) break;
-                    const uint64_t dks = dk + st * kKStage;
+            if (ok) {
+                for (int t = 0; t < kTcTiles; ++t)
+                    if (n_t[t] > 0) issue_qk(t, 0);
+                umma_commit(smem_u32(&k_empty[0]));
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int st = j % kTcStages, st1 = (j + 1) % kTcStages;
+                const bool more = j + 1 < n_tiles;
+                if (!mbar_wait(smem_u32(&v_full[st]), (j / kTcStages) & 1, err)) break;
+                if (more && !mbar_wait(smem_u32(&k_full[st1]), ((j + 1) / kTcStages) & 1, err)) break;
 #pragma unroll
-                    for (int t = 0; t < kTcTiles; ++t) {
-                        if (j >= n_t[t]) continue;
-                        if (j >= 2 && !mbar_wait(smem_u32(&s_free[t][sb]), ((j >> 1) - 1) & 1, err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d_s = tmem + Ly::kTmemS + t * 128 + sb * kTcKeys;
-                        const uint64_t dqt = dq + t * kQTile;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
-                            const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
-                            umma_f16(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
-                        }
-                        umma_commit(smem_u32(&s_full[t][sb]));
+                for (int t = 0; t < kTcTiles; ++t) {
+                    if (j >= n_t[t]) continue;
+                    if (!mbar_wait(smem_u32(&p_full[t]), j & 1, err)) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
-                    umma_commit(smem_u32(&k_empty[st]));
+                    tc_fence_after();
+                    issue_pv(t, j);
+                    if (j + 1 < n_t[t]) issue_qk(t, j + 1);
                 }
-                if (j >= 1) {
-                    const int jp = j - 1, stp = jp % kTcStages;
-                    if (!mbar_wait(smem_u32(&v_full[stp]), (jp / kTcStages) & 1, err)) break;
-                    const uint64_t dvs = dv + stp * kKStage;
-#pragma unroll
-                    for (int t = 0; t < kTcTiles; ++t) {
-                        if (jp >= n_t[t]) continue;
-                        if (!mbar_wait(smem_u32(&p_full[t][jp & 1]), (jp >> 1) & 1, err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d_o = tmem + Ly::kTmemO + t * D;
-                        const uint32_t a_p = tmem + Ly::kTmemS + t * 128 + (jp & 1) * kTcKeys;
-#pragma unroll
-                        for (int ks = 0; ks < kTcKeys / 16; ++ks) {   // 16 keys = 8 columns
-                            umma_f16_ts(d_o, a_p + ks * 8, dvs + ks * (2048 >> 4), kIdescPV,
-                                        (jp > 0 || ks > 0) ? 1u : 0u);
-                            umma_f16_ts(d_o, a_p + 32 + ks * 8, dvs + ks * (2048 >> 4), kIdescPV, 1u);
-                        }
-                        umma_commit(smem_u32(&pv_done[t][jp & 1]));
-                    }
-                    if (!ok) break;
-                    umma_commit(smem_u32(&v_empty[stp]));
-                }
+                if (!ok) break;
+                umma_commit(smem_u32(&v_empty[st]));
+                if (more) umma_commit(smem_u32(&k_empty[st1]));
             }
         }
     } else {
         // ------------------------------------------------ softmax warps 0-7
         // Warp w serves tile t = w / 4 and reads TMEM lanes 32*(w % 4) .. +31:
-        // thread = M row, all 64 keys of every key tile, all D columns of O.
+        // thread = M row, all 128 keys of every key tile, all D columns of O.
         const int t = warp >> 2, quarter = warp & 3;
         const int rr = quarter * 32 + lane;                 // M row in the tile = TMEM lane
         const int grow = row0 + t * kTcRows + rr;
@@ -323,35 +316,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         float m_raw = -INFINITY, l = 0.f;
         bool broken = false;
         for (int j = 0; j < nt; ++j) {
-            const int sb = j & 1;
-            const bool ok = mbar_wait(smem_u32(&s_full[t][sb]), (j >> 1) & 1, err);
+            const bool ok = mbar_wait(smem_u32(&s_full[t]), j & 1, err);
             if (!__all_sync(0xffffffffu, ok)) {
                 broken = true;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[kTcKeys];
-            tmem_ld32(lane_addr + s_col + sb * kTcKeys, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(lane_addr + s_col + sb * kTcKeys + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_free[t][sb]));
-
-            // scores stay raw (unscaled) until the exponent: the max is taken on
-            // raw values and p = 2^(s*c - m*c) is one FFMA and one EX2
+            // S_t(j) done implies P_t(j - 1) V done (issued earlier, committed
+            // in order): O may be rescaled now, and P may overwrite S.
             const int key0 = j * kTcKeys;
             const bool full_tile = key0 + kTcKeys - 1 <= warp_min_pos;
+
+            // pass 1: row max over the 128 raw scores (scores stay unscaled until
+            // the exponent: p = 2^(s*c - m*c) is one FFMA and one EX2)
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (full_tile) {
 #pragma unroll
-                for (int i = 0; i < kTcKeys; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
-            } else {
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sr[64];
+                tmem_ld32(lane_addr + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(lane_addr + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld_wait();
+                if (full_tile) {
 #pragma unroll
-                for (int i = 0; i < kTcKeys; ++i) {
-                    const float z = (key0 + i <= p_abs) ? __uint_as_float(sr[i]) : -INFINITY;
-                    sr[i] = __float_as_uint(z);
-                    m4[i & 3] = fmaxf(m4[i & 3], z);
+                    for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (key0 + h * 64 + i <= p_abs) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
                 }
             }
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -367,59 +358,53 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 l *= fac;
             }
             const float neg_mc = -m_raw * scale_log2;
-
-            // O is rescaled only when the reference max moved: that needs the
-            // previous P V done (no MMA writes O meanwhile)
             if (j >= 1 && __any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
-                const bool ok2 = mbar_wait(smem_u32(&pv_done[t][(j - 1) & 1]), ((j - 1) >> 1) & 1, err);
-                if (!__all_sync(0xffffffffu, ok2)) {
-                    broken = true;
-                    break;
-                }
-                tc_fence_after();
-                {
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_addr + o_col + c0, o);
-                        tmem_ld_wait();
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + o_col + c0, o);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
-                        tmem_st32(lane_addr + o_col + c0, o);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
+                    tmem_st32(lane_addr + o_col + c0, o);
                 }
             }
 
-            // P: exponent, row sum, hi/lo split, written over S_t[sb] in TMEM
-            // (the scores were read above; their MMA ordered before this P V)
+            // pass 2, per 64 keys: exponent, row sum, hi/lo split, written over
+            // those keys' own score columns (hi, then lo)
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t ph[kTcKeys / 2], pl[kTcKeys / 2];
-            if (full_tile) {
 #pragma unroll
-                for (int i = 0; i < kTcKeys / 2; ++i) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
-                    s4[i & 3] += p0 + p1;
-                    split_trunc<T>(p0, p1, ph[i], pl[i]);
-                }
-            } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sr[64];
+                tmem_ld32(lane_addr + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(lane_addr + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld_wait();
+                uint32_t ph[32], pl[32];
+                if (full_tile) {
 #pragma unroll
-                for (int i = 0; i < kTcKeys / 2; ++i) {
-                    const float s0 = __uint_as_float(sr[2 * i]), s1 = __uint_as_float(sr[2 * i + 1]);
-                    const float p0 = s0 == -INFINITY ? 0.f : fast_exp2(fmaf(s0, scale_log2, neg_mc));
-                    const float p1 = s1 == -INFINITY ? 0.f : fast_exp2(fmaf(s1, scale_log2, neg_mc));
-                    s4[i & 3] += p0 + p1;
-                    split_trunc<T>(p0, p1, ph[i], pl[i]);
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
+                        s4[i & 3] += p0 + p1;
+                        split_trunc<T>(p0, p1, ph[i], pl[i]);
+                    }
+                } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int k = key0 + h * 64 + 2 * i;
+                        const float p0 = k <= p_abs ? fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc)) : 0.f;
+                        const float p1 = k + 1 <= p_abs ? fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc)) : 0.f;
+                        s4[i & 3] += p0 + p1;
+                        split_trunc<T>(p0, p1, ph[i], pl[i]);
+                    }
                 }
+                tmem_st32(lane_addr + s_col + h * 64, ph);
+                tmem_st32(lane_addr + s_col + h * 64 + 32, pl);
             }
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-            tmem_st32(lane_addr + s_col + sb * kTcKeys, ph);
-            tmem_st32(lane_addr + s_col + sb * kTcKeys + 32, pl);
             tmem_st_wait();
 
-            const int tkey0 = j * kTcKeys;
-            if (tkey0 + kTcKeys > L) {
+            if (key0 + kTcKeys > L) {
                 // keys at or past L (only in the request's last key tile) may hold
                 // anything, even NaN: zero those V rows so P = 0 keeps them out,
                 // after the tile's V has landed.  Both tiles' rows may do this for
@@ -429,7 +414,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     broken = true;
                     break;
                 }
-                const int valid_rows = max(0, L - tkey0);
+                const int valid_rows = max(0, L - key0);
                 const int per_half = (kTcKeys - valid_rows) * 8;      // 16-byte pieces
                 const uint32_t vb = sbase + Ly::kOffV + (j % kTcStages) * Ly::kKBytes;
                 for (int i = quarter * 32 + lane; i < per_half * Ly::kHalves; i += 4 * 32) {
@@ -437,16 +422,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     const int rem = i - hx * per_half;
                     st_shared_v4(vb + hx * (kTcKeys * 128) + valid_rows * 128 + rem * 16, 0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
             }
-            if (tkey0 + kTcKeys > L) fence_proxy_async_smem();   // the zeroed V rows
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full[t][sb]));
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[t]));
         }
 
         // ------------------------------------------------ epilogue: O / l
         if (!broken && nt > 0) {
-            const bool ok = mbar_wait(smem_u32(&pv_done[t][(nt - 1) & 1]), ((nt - 1) >> 1) & 1, err);
+            const bool ok = mbar_wait(smem_u32(&pv_done[t]), (nt - 1) & 1, err);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float inv = 1.f / l;
