@@ -17,8 +17,11 @@
 //             into TMEM, O_t += P_t V (M 128, N = d, K 128) into TMEM, in the
 //             order P_A(j) V, S_A(j+1), P_B(j) V, S_B(j+1): while one tile's rows
 //             run their softmax the tensor cores work on the other tile;
-//   warps 0-3 (tile A), 4-7 (tile B): one thread per M row reads its 128
-//             scores from TMEM, applies the causal mask on absolute positions,
+//   warps 0-15: two threads per M row of a tile (warps 0-3 and 8-11 tile A,
+//             4-7 and 12-15 tile B), each with 64 of a key tile's 128 keys and
+//             half of O's columns; the pair swaps partial row maxima through
+//             shared memory and a named barrier.  A row reads its scores from
+//             TMEM, applies the causal mask on absolute positions,
 //             runs the online softmax in base 2 with lazy rescaling (O in TMEM
 //             is rescaled only when the running max grows by more than 2^8),
 //             and writes P back over its scores in TMEM as hi + lo bf16/fp16
@@ -39,7 +42,7 @@ constexpr int kTcRows = 128;      // M rows per tile
 constexpr int kTcTiles = 2;       // tiles per CTA (A, B)
 constexpr int kTcKeys = 128;      // keys per key tile
 constexpr int kTcStages = 2;      // K/V ring depth
-constexpr int kSoftmaxWarps = 4 * kTcTiles;
+constexpr int kSoftmaxWarps = 8 * kTcTiles;   // two threads per row of each tile
 constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1, kMmaWarp = kSoftmaxWarps + 2;
 constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;   // softmax, K producer, V producer, MMA
 constexpr uint32_t kTmemCols = 512;   // S/P_A [0,128) S/P_B [128,256) O_A, O_B from 256
@@ -53,8 +56,8 @@ struct PfLayout {
     static constexpr uint32_t kOffK = kOffQ + kTcTiles * kQBytes; // K ring
     static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
     static constexpr uint32_t kDynBytes = kOffV + kTcStages * kKBytes + 1024;
-    // S_t at t * 128; P_t overwrites it, keys 64h .. 64h+63 as hi in columns
-    // 64h .. 64h+31 and lo in 64h+32 .. 64h+63 (two 16-bit values per column)
+    // S_t at t * 128; P_t overwrites it, keys 32c .. 32c+31 as hi in columns
+    // 32c .. 32c+15 and lo in 32c+16 .. 32c+31 (two 16-bit values per column)
     static constexpr uint32_t kTmemS = 0;
     static constexpr uint32_t kTmemO = 256;                       // + t * D
     static_assert(kDynBytes <= 232448, "shared memory per CTA");
@@ -137,6 +140,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
     __shared__ __align__(8) uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles], q_ready;
     __shared__ uint32_t s_tmem;
+    // partial row maxima of the two threads of a row (double-buffered by key
+    // tile), a "stop" flag beside each, and the partial row sums at the end
+    __shared__ float xmax[2][kTcTiles][2][kTcRows];
+    __shared__ int xstop[2][kTcTiles][2][kTcRows];
+    __shared__ float xsum[kTcTiles][2][kTcRows];
+    __shared__ int xstop_end[kTcTiles][2][kTcRows];
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -152,7 +161,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         for (int t = 0; t < kTcTiles; ++t) {
             mbar_init(smem_u32(&s_full[t]), 1);
-            mbar_init(smem_u32(&p_full[t]), 4);
+            mbar_init(smem_u32(&p_full[t]), 8);
             mbar_init(smem_u32(&pv_done[t]), 1);
         }
         mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
@@ -237,10 +246,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const uint32_t a_p = tmem + Ly::kTmemS + t * 128;
 #pragma unroll
                 for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-                    const uint32_t col = (ks >> 2) * 64 + (ks & 3) * 8;   // 16 keys = 8 columns
+                    // keys 16 ks .. +15: 32-key chunk ks / 2 holds hi in its first
+                    // 16 columns and lo in the next 16 (16 keys = 8 columns)
+                    const uint32_t col = (ks >> 1) * 32 + (ks & 1) * 8;
                     umma_f16_ts(d_o, a_p + col, dvs + ks * (2048 >> 4), kIdescPV,
                                 (j > 0 || ks > 0) ? 1u : 0u);
-                    umma_f16_ts(d_o, a_p + col + 32, dvs + ks * (2048 >> 4), kIdescPV, 1u);
+                    umma_f16_ts(d_o, a_p + col + 16, dvs + ks * (2048 >> 4), kIdescPV, 1u);
                 }
                 umma_commit(smem_u32(&pv_done[t]));
             };
@@ -274,10 +285,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
         }
     } else {
-        // ------------------------------------------------ softmax warps 0-7
-        // Warp w serves tile t = w / 4 and reads TMEM lanes 32*(w % 4) .. +31:
-        // thread = M row, all 128 keys of every key tile, all D columns of O.
-        const int t = warp >> 2, quarter = warp & 3;
+        // ------------------------------------------------ softmax warps 0-15
+        // Warp w serves tile t = (w / 4) % 2, half hf = w / 8 of every key
+        // tile's keys and of O's columns, and reads TMEM lanes 32*(w % 4) ..
+        // +31.  The two warps of a row pair meet once per key tile at a named
+        // barrier; no warp leaves the loop except right after that meeting,
+        // when both see the same stop flag, so neither can wait there alone.
+        const int t = (warp >> 2) & 1, quarter = warp & 3, hf = warp >> 3;
         const int rr = quarter * 32 + lane;                 // M row in the tile = TMEM lane
         const int grow = row0 + t * kTcRows + rr;
         const bool valid = grow < rows_total;
@@ -285,12 +299,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int head = kvh * group + (valid ? grow - (grow / group) * group : 0);
         const int p_abs = valid ? ctx0 + pos_local : L - 1;   // padding rows see every key
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t s_col = Ly::kTmemS + t * 128, o_col = Ly::kTmemO + t * D;
+        const uint32_t s_col = Ly::kTmemS + t * 128 + hf * 64;      // this thread's 64 keys
+        const uint32_t o_col = Ly::kTmemO + t * D + hf * (D / 2);   // this thread's O columns
+        const int bar_id = 1 + t * 4 + quarter;                      // the pair's named barrier
         const int nt = n_t[t];
 
-        // Q row -> shared memory, 128-byte swizzled rows.  A negative scale is
-        // applied as -Q and |scale| (an exact sign flip), so the raw-score max
-        // is the scaled max.
+        // Q row (this thread's half of it) -> shared memory, 128-byte swizzled
+        // rows.  A negative scale is applied as -Q and |scale| (an exact sign
+        // flip), so the raw-score max is the scaled max.
         const uint32_t qsign = scale_log2 < 0.f ? 0x80008000u : 0u;
         scale_log2 = fabsf(scale_log2);
         {
@@ -298,7 +314,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 q + (static_cast<int64_t>(qs + pos_local) * n_q + head) * D);
             const uint32_t qbase = sbase + Ly::kOffQ + t * Ly::kQBytes;
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
+            for (int cc = 0; cc < D / 16; ++cc) {
+                const int c = hf * (D / 16) + cc;
                 uint4 v = valid ? __ldg(qp + c) : make_uint4(0, 0, 0, 0);
                 v.x ^= qsign; v.y ^= qsign; v.z ^= qsign; v.w ^= qsign;
                 const uint32_t addr = qbase + (c >> 3) * (kTcRows * 128) + rr * 128 +
@@ -314,38 +331,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int wrow = row0 + t * kTcRows + quarter * 32;
         const int warp_min_pos = wrow < rows_total ? ctx0 + wrow / group : L - 1;
         float m_raw = -INFINITY, l = 0.f;
-        bool broken = false;
+        bool stop = false;   // a wait of this warp ran out
+        bool quit = false;   // the pair left the loop together
         for (int j = 0; j < nt; ++j) {
-            const bool ok = mbar_wait(smem_u32(&s_full[t]), j & 1, err);
-            if (!__all_sync(0xffffffffu, ok)) {
-                broken = true;
-                break;
-            }
-            tc_fence_after();
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t]), j & 1, err));
+            if (ok) tc_fence_after();
             // S_t(j) done implies P_t(j - 1) V done (issued earlier, committed
             // in order): O may be rescaled now, and P may overwrite S.
-            const int key0 = j * kTcKeys;
+            const int key0 = j * kTcKeys, hkey0 = key0 + hf * 64;
             const bool full_tile = key0 + kTcKeys - 1 <= warp_min_pos;
 
-            // pass 1: row max over the 128 raw scores (scores stay unscaled until
-            // the exponent: p = 2^(s*c - m*c) is one FFMA and one EX2)
+            // pass 1: max over this thread's 64 raw scores, swapped with the
+            // partner's (scores stay unscaled until the exponent: p =
+            // 2^(s*c - m*c) is one FFMA and one EX2)
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (ok) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sr[64];
-                tmem_ld32(lane_addr + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(lane_addr + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                tmem_ld_wait();
-                if (full_tile) {
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t sr[32];
+                    tmem_ld32(lane_addr + s_col + h2 * 32, sr);
+                    tmem_ld_wait();
+                    if (full_tile) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
-                } else {
+                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (key0 + h * 64 + i <= p_abs) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+                        for (int i = 0; i < 32; ++i)
+                            if (hkey0 + h2 * 32 + i <= p_abs) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+                    }
                 }
             }
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            xmax[j & 1][t][hf][rr] = mx;
+            xstop[j & 1][t][hf][rr] = (!ok || stop) ? 1 : 0;
+            named_bar_sync(bar_id, 64);
+            mx = fmaxf(mx, xmax[j & 1][t][hf ^ 1][rr]);
+            stop = stop || !ok || xstop[j & 1][t][hf ^ 1][rr] != 0;
+            if (__any_sync(0xffffffffu, stop)) {   // the partner warp sees the same flags
+                quit = true;
+                break;
+            }
 
             // lazy: move the reference max only when the first tile sets it or
             // the max grew by more than 2^8 (written so that scale 0 stays finite)
@@ -360,7 +385,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const float neg_mc = -m_raw * scale_log2;
             if (j >= 1 && __any_sync(0xffffffffu, resc)) {   // TMEM access is warp-wide
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
                     uint32_t o[32];
                     tmem_ld32(lane_addr + o_col + c0, o);
                     tmem_ld_wait();
@@ -370,19 +395,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
             }
 
-            // pass 2, per 64 keys: exponent, row sum, hi/lo split, written over
-            // those keys' own score columns (hi, then lo)
+            // pass 2, per 32 keys: exponent, row sum, hi/lo split, written over
+            // those 32 keys' own score columns (hi in the first 16, lo in the
+            // next 16), so no score is overwritten before it is read
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t sr[64];
-                tmem_ld32(lane_addr + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(lane_addr + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t sr[32];
+                tmem_ld32(lane_addr + s_col + h2 * 32, sr);
                 tmem_ld_wait();
-                uint32_t ph[32], pl[32];
+                uint32_t ph[16], pl[16];
                 if (full_tile) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
                         const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
                         s4[i & 3] += p0 + p1;
@@ -390,16 +415,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     }
                 } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int k = key0 + h * 64 + 2 * i;
+                    for (int i = 0; i < 16; ++i) {
+                        const int k = hkey0 + h2 * 32 + 2 * i;
                         const float p0 = k <= p_abs ? fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc)) : 0.f;
                         const float p1 = k + 1 <= p_abs ? fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc)) : 0.f;
                         s4[i & 3] += p0 + p1;
                         split_trunc<T>(p0, p1, ph[i], pl[i]);
                     }
                 }
-                tmem_st32(lane_addr + s_col + h * 64, ph);
-                tmem_st32(lane_addr + s_col + h * 64 + 32, pl);
+                tmem_st16(lane_addr + s_col + h2 * 32, ph);        // over the scores
+                tmem_st16(lane_addr + s_col + h2 * 32 + 16, pl);   // just read
+
             }
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             tmem_st_wait();
@@ -408,21 +434,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 // keys at or past L (only in the request's last key tile) may hold
                 // anything, even NaN: zero those V rows so P = 0 keeps them out,
                 // after the tile's V has landed.  Both tiles' rows may do this for
-                // the same key tile; they write the same zeros.
-                const bool okv = mbar_wait(smem_u32(&v_full[j % kTcStages]), (j / kTcStages) & 1, err);
-                if (!__all_sync(0xffffffffu, okv)) {
-                    broken = true;
-                    break;
+                // the same key tile; they write the same zeros.  A wait that runs
+                // out skips the work; the pair stops at its next meeting.
+                if (__all_sync(0xffffffffu, mbar_wait(smem_u32(&v_full[j % kTcStages]), (j / kTcStages) & 1, err))) {
+                    const int valid_rows = max(0, L - key0);
+                    const int per_half = (kTcKeys - valid_rows) * 8;      // 16-byte pieces
+                    const uint32_t vb = sbase + Ly::kOffV + (j % kTcStages) * Ly::kKBytes;
+                    for (int i = (hf * 4 + quarter) * 32 + lane; i < per_half * Ly::kHalves; i += 8 * 32) {
+                        const int hx = i / per_half;
+                        const int rem = i - hx * per_half;
+                        st_shared_v4(vb + hx * (kTcKeys * 128) + valid_rows * 128 + rem * 16, 0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                } else {
+                    stop = true;
                 }
-                const int valid_rows = max(0, L - key0);
-                const int per_half = (kTcKeys - valid_rows) * 8;      // 16-byte pieces
-                const uint32_t vb = sbase + Ly::kOffV + (j % kTcStages) * Ly::kKBytes;
-                for (int i = quarter * 32 + lane; i < per_half * Ly::kHalves; i += 4 * 32) {
-                    const int hx = i / per_half;
-                    const int rem = i - hx * per_half;
-                    st_shared_v4(vb + hx * (kTcKeys * 128) + valid_rows * 128 + rem * 16, 0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
             }
             tc_fence_before();
             __syncwarp();
@@ -430,21 +456,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
 
         // ------------------------------------------------ epilogue: O / l
-        if (!broken && nt > 0) {
-            const bool ok = mbar_wait(smem_u32(&pv_done[t]), (nt - 1) & 1, err);
+        // the pair meets once more, to add its partial sums, unless it left
+        // the loop together; a late failure of either warp skips the output
+        if (!quit && nt > 0) {
+            xsum[t][hf][rr] = l;
+            xstop_end[t][hf][rr] = stop ? 1 : 0;
+            named_bar_sync(bar_id, 64);
+            const float lsum = l + xsum[t][hf ^ 1][rr];
+            stop = stop || xstop_end[t][hf ^ 1][rr] != 0;
+            const bool ok = !__any_sync(0xffffffffu, stop) &&
+                            mbar_wait(smem_u32(&pv_done[t]), (nt - 1) & 1, err);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                const float inv = 1.f / l;
+                const float inv = 1.f / lsum;
                 const int64_t obase = (static_cast<int64_t>(qs + pos_local) * n_q + head) * D;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
                     uint32_t o[32];
                     tmem_ld32(lane_addr + o_col + c0, o);
                     tmem_ld_wait();
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * inv;
-                    if (valid) store_row<T>(out, obase, c0, v, 32, out_dtype);
+                    if (valid) store_row<T>(out, obase, hf * (D / 2) + c0, v, 32, out_dtype);
                 }
             }
         }
