@@ -74,27 +74,30 @@ constexpr int decode_dyn_avail(bool fp8)
 // Ring depth per warp: about `budget` bytes of K+V in flight per warp, at least
 // 2 stages; when a separate combine buffer fits beside a ring of at least 2
 // stages, the ring is cut to what fits beside it.
-template <typename T, int D, bool FP8>
+template <typename T, int D, bool FP8, int RU = 8>
 constexpr int decode_stages()
 {
     constexpr int stage = 2 * kRows * D * (FP8 ? 1 : static_cast<int>(sizeof(T)));
     constexpr int budget = FP8 ? 12288 : 24576;
     constexpr int ns = budget / stage > 2 ? budget / stage : 2;
-    constexpr int red = kDecWarps * 8 * (D + 2) * 4;
+    constexpr int red = kDecWarps * RU * (D + 2) * 4;
     constexpr int fit = (decode_dyn_avail(FP8) - red) / (kDecWarps * stage);
     return kPreferSepRed && fit >= 2 ? (fit < ns ? fit : ns) : ns;
 }
 
 // FP8 pools: a stage holds 16 rows of E4M3 K codes (swizzled rows of D bytes)
 // and the matching D x 16 tile of the transposed V codes.
-template <typename T, int D, int NS, bool FP8 = false>
+// RU: rows of the MMA tile a work unit fills (8 = one sub-group of up to 8
+// heads with P's hi/lo halves in rows 0-7 / 8-15; 16 = sixteen (head, query)
+// rows, P's halves in two MMAs).
+template <typename T, int D, int NS, bool FP8 = false, int RU = 8>
 struct DecodeCfg {
     static constexpr int kElem = FP8 ? 1 : static_cast<int>(sizeof(T));
     static constexpr int kSlabBytes = kRows * D * kElem;    // 16 rows of K or V as stored
     static constexpr int kStageBytes = 2 * kSlabBytes;
     static constexpr int kWarpBytes = NS * kStageBytes;
     static constexpr int kRingBytes = kDecWarps * kWarpBytes;
-    static constexpr int kReduceBytes = kDecWarps * 8 * (D + 2) * 4;
+    static constexpr int kReduceBytes = kDecWarps * RU * (D + 2) * 4;
     // the combine buffer sits after the rings when both fit, else it aliases them
     static constexpr bool kSepRed =
         kPreferSepRed && kRingBytes + kReduceBytes <= decode_dyn_avail(FP8);
@@ -129,7 +132,7 @@ __device__ __forceinline__ uint32_t q_pair<__nv_bfloat16, __half>(const __nv_bfl
     return Cvt<__half>::pack(f.x, f.y);
 }
 
-template <typename T, typename QT, int D, int BS, int NS, bool FP8, bool MQ>
+template <typename T, typename QT, int D, int BS, int NS, bool FP8, bool MQ, int RU = 8>
 __global__ void __launch_bounds__(kDecWarps * 32, decode_ctas_per_sm(FP8))
 decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
@@ -139,8 +142,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                   float* __restrict__ ws_ml, float* __restrict__ ws_acc, int part_tokens,
                   int max_parts, unsigned* __restrict__ ticket, unsigned* err)
 {
-    using Cfg = DecodeCfg<T, D, NS, FP8>;
+    using Cfg = DecodeCfg<T, D, NS, FP8, RU>;
     static_assert(!FP8 || std::is_same<T, __half>::value, "FP8 pools compute in fp16");
+    constexpr bool R16 = RU == 16;
+    static_assert(RU == 8 || (RU == 16 && MQ && !FP8), "16-row units: multi-query, 16-bit pools");
     constexpr int kHalves = D / 64;           // 64-column halves (one 128-byte swizzled row each)
     constexpr int kHalfTile = kRows * 128;
     constexpr int kCPB = BS / kRows;          // stages per block
@@ -151,7 +156,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     __shared__ int s_blk[2][kMaxPartBlocks];   // this unit's and the next unit's block ids
     __shared__ int s_total;
     __shared__ long long s_next;
-    __shared__ long long s_rowoff[8];   // MQ: output row of each row of the sub-group
+    __shared__ long long s_rowoff[RU];   // MQ: output row of each row of the sub-group
     __shared__ __align__(8) uint64_t s_bar[kDecWarps * NS];
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -159,9 +164,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // a KV head serves group x nq rows (head-major: row = head * nq + query),
-    // taken 8 at a time; plain decode (MQ false) has nq = 1 at compile time
+    // taken RU at a time; plain decode (MQ false) has nq = 1 at compile time
     const int nq = MQ ? nq_arg : 1;
-    const int n_sub = (group * nq + 7) >> 3;
+    const int n_sub = (group * nq + RU - 1) / RU;
     const int n_groups = n_kv * n_sub;
     const bool use_prefix = num_seqs <= kPrefixCap;
 
@@ -254,8 +259,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         x.kvh = grp / n_sub;
         const int sub = grp - x.kvh * n_sub;
         x.h0 = x.kvh * group;                         // first query head of the KV head
-        x.r0 = sub * 8;                               // first row of the sub-group
-        x.nh = min(8, group * nq - x.r0);             // rows in the sub-group
+        x.r0 = sub * RU;                              // first row of the sub-group
+        x.nh = min(RU, group * nq - x.r0);            // rows in the sub-group
         const int tok1 = min(x.L, x.tok0 + part_tokens);
         x.nblk = (tok1 - x.tok0 + BS - 1) / BS;
         x.nchunk = (tok1 - x.tok0 + kRows - 1) / kRows;
@@ -275,11 +280,25 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         return b;
     };
-    // query fragments of unit x: rows 0-7 = heads of the sub-group, rows 8-15 zero
+    // query fragments of unit x: rows 0-7 = rows g of the sub-group; rows 8-15
+    // zero (RU 8) or rows g + 8 (RU 16, in qb)
     uint32_t qa[D / 16][2];
+    uint32_t qb[R16 ? D / 16 : 1][2];
     auto load_q = [&](const Unit& x) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+            if constexpr (R16) {
+                if (g + 8 < x.nh) {
+                    const int hh = (x.r0 + g + 8) / nq, qi = x.r0 + g + 8 - hh * nq;
+                    const QT* row =
+                        q + ((static_cast<int64_t>(x.s) * nq + qi) * n_q + x.h0 + hh) * D + kk * 16;
+                    qb[kk][0] = q_pair<QT, T>(row + 2 * t4);
+                    qb[kk][1] = q_pair<QT, T>(row + 2 * t4 + 8);
+                } else {
+                    qb[kk][0] = 0u;
+                    qb[kk][1] = 0u;
+                }
+            }
             if (g < x.nh) {
                 const int hh = (x.r0 + g) / nq, qi = x.r0 + g - hh * nq;
                 const QT* row =
@@ -324,9 +343,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         return x.nchunk > warp ? (x.nchunk - warp + kDecWarps - 1) / kDecWarps : 0;
     };
 
-    float* red_o = reinterpret_cast<float*>(smem + Cfg::kRedOffset);   // [warps][8][D]
-    float* red_m = red_o + kDecWarps * 8 * D;                           // [warps][8]
-    float* red_l = red_m + kDecWarps * 8;                               // [warps][8]
+    float* red_o = reinterpret_cast<float*>(smem + Cfg::kRedOffset);   // [warps][RU][D]
+    float* red_m = red_o + kDecWarps * RU * D;                          // [warps][RU]
+    float* red_l = red_m + kDecWarps * RU;                              // [warps][RU]
 
     // ---- the first unit: ids checked before any load is issued
     int64_t u = blockIdx.x;
@@ -346,7 +365,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     bool issued = false;                              // its first stages are in flight
 
     float o[D / 8][4];
-    float m_run, l_run;
+    float m_run, l_run;     // row g
+    float m_run1, l_run1;   // row g + 8 (RU 16)
     while (u < units) {
         const Unit nx = describe(un);
         // the next unit's block ids: in flight while this unit streams
@@ -357,6 +377,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const int h0 = cu.h0, r0 = cu.r0, nh = cu.nh, nchunk = cu.nchunk, nparts = cu.nparts;
         // keys this thread's row may see: query qi of nq sits at L - nq + qi
         const int lim = g < nh ? L - nq + (r0 + g) % nq + 1 : L;
+        const int lim1 = (R16 && g + 8 < nh) ? L - nq + (r0 + g + 8) % nq + 1 : L;
         int timed_out = 0;
         if (cu.live) {
             // ---- per-warp TMA ring over the partition's 16-row stages --------
@@ -369,6 +390,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
             for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             m_run = -INFINITY;
+            m_run1 = -INFINITY;
+            l_run1 = 0.f;
             l_run = 0.f;
 
             for (int k = 0; k < my_n; ++k) {
@@ -450,8 +473,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                                                   (((chunk & 7) ^ (r & 7)) << 4);
                             uint32_t b0, b1, b2, b3;
                             ldsm_x4(addr, b0, b1, b2, b3);
-                            const uint32_t a0[4] = {qa[kc][0], 0u, qa[kc][1], 0u};
-                            const uint32_t a1[4] = {qa[kc + 1][0], 0u, qa[kc + 1][1], 0u};
+                            const uint32_t a0[4] = {qa[kc][0], R16 ? qb[R16 ? kc : 0][0] : 0u, qa[kc][1],
+                                                    R16 ? qb[R16 ? kc : 0][1] : 0u};
+                            const uint32_t a1[4] = {qa[kc + 1][0], R16 ? qb[R16 ? kc + 1 : 0][0] : 0u,
+                                                    qa[kc + 1][1], R16 ? qb[R16 ? kc + 1 : 0][1] : 0u};
                             MmaOp<T>::run(sc[nt], a0, b0, b1);
                             MmaOp<T>::run(sc[nt], a1, b2, b3);
                         }
@@ -475,33 +500,62 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 // a row with no visible key so far (several queries per sequence)
                 // keeps m = -inf: exponents are then taken against 0, giving 0
                 const float m_use = (MQ && m_new == -INFINITY) ? 0.f : m_new;
+                float m_new1 = -INFINITY, m_use1 = 0.f;
+                if constexpr (R16) {   // the second row of this thread, same steps
+                    float mx1 = -INFINITY;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 2; e < 4; ++e) {
+                            const int p = pos0 + nt * 8 + 2 * t4 + e - 2;
+                            const float z = p < lim1 ? sc[nt][e] * scale_log2 : -INFINITY;
+                            sc[nt][e] = z;
+                            mx1 = fmaxf(mx1, z);
+                        }
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                    m_new1 = fmaxf(m_run1, mx1);
+                    m_use1 = m_new1 == -INFINITY ? 0.f : m_new1;
+                }
                 // rescale only when some row's running max moved (warp-uniform
                 // branch; after the first stages the max rarely moves).  The first
                 // stage has m_run = -inf: alpha = 0 clears the (zero) state.
-                if (__any_sync(0xffffffffu, m_new != m_run)) {
+                if (__any_sync(0xffffffffu, m_new != m_run || (R16 && m_new1 != m_run1))) {
                     const float alpha = fast_exp2(m_run - m_use);
+                    const float alpha1 = R16 ? fast_exp2(m_run1 - m_use1) : alpha;
                     l_run *= alpha;
+                    l_run1 *= alpha1;
 #pragma unroll
                     for (int i = 0; i < D / 8; ++i) {
-                        o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha; o[i][3] *= alpha;
+                        o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha1; o[i][3] *= alpha1;
                     }
                 }
                 m_run = m_new;
-                float psum = 0.f;
+                m_run1 = m_new1;
+                float psum = 0.f, psum1 = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float p = fast_exp2(sc[nt][e] - m_use);
+                    for (int e = 0; e < (R16 ? 4 : 2); ++e) {
+                        const float p = fast_exp2(sc[nt][e] - (e < 2 ? m_use : m_use1));
                         sc[nt][e] = p;
-                        psum += p;
+                        if (e < 2) psum += p; else psum1 += p;
                     }
                 l_run += psum;
+                l_run1 += psum1;
 
-                // O += P V, P as hi (rows 0-7) + lo (rows 8-15)
-                uint32_t pa[4];
-                split_pair<T>(sc[0][0], sc[0][1], pa[0], pa[1]);
-                split_pair<T>(sc[1][0], sc[1][1], pa[2], pa[3]);
+                // O += P V, P as hi (rows 0-7) + lo (rows 8-15); RU 16: rows g and
+                // g + 8 both real, hi in pa and lo in pb, two MMAs
+                uint32_t pa[4], pb[4];
+                if constexpr (R16) {
+                    split_pair<T>(sc[0][0], sc[0][1], pa[0], pb[0]);
+                    split_pair<T>(sc[0][2], sc[0][3], pa[1], pb[1]);
+                    split_pair<T>(sc[1][0], sc[1][1], pa[2], pb[2]);
+                    split_pair<T>(sc[1][2], sc[1][3], pa[3], pb[3]);
+                } else {
+                    split_pair<T>(sc[0][0], sc[0][1], pa[0], pa[1]);
+                    split_pair<T>(sc[1][0], sc[1][1], pa[2], pa[3]);
+                }
                 if constexpr (FP8) {
                     // transposed V tile: row d holds tokens 0..15; a fragment word is
                     // tokens 4*t4 .. 4*t4+3 of row d, the k order P is in
@@ -530,6 +584,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         ldsm_x4_t(addr, b0, b1, b2, b3);
                         MmaOp<T>::run(o[nt], pa, b0, b1);
                         MmaOp<T>::run(o[nt + 1], pa, b2, b3);
+                        if constexpr (R16) {
+                            MmaOp<T>::run(o[nt], pb, b0, b1);
+                            MmaOp<T>::run(o[nt + 1], pb, b2, b3);
+                        }
                     }
                 }
 
@@ -543,16 +601,31 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             // ---- this warp's share of the combine
             l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
             l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+            if constexpr (R16) {
+                l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 1);
+                l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 2);
+            }
             if constexpr (Cfg::kSepRed) {
 #pragma unroll
                 for (int nt = 0; nt < D / 8; ++nt) {
-                    float* dst = red_o + (warp * 8 + g) * D + nt * 8 + 2 * t4;
-                    dst[0] = o[nt][0] + o[nt][2];
-                    dst[1] = o[nt][1] + o[nt][3];
+                    float* dst = red_o + (warp * RU + g) * D + nt * 8 + 2 * t4;
+                    if constexpr (R16) {
+                        dst[0] = o[nt][0];
+                        dst[1] = o[nt][1];
+                        dst[8 * D] = o[nt][2];           // row g + 8
+                        dst[8 * D + 1] = o[nt][3];
+                    } else {
+                        dst[0] = o[nt][0] + o[nt][2];
+                        dst[1] = o[nt][1] + o[nt][3];
+                    }
                 }
                 if (t4 == 0) {
-                    red_m[warp * 8 + g] = m_run;
-                    red_l[warp * 8 + g] = l_run;
+                    red_m[warp * RU + g] = m_run;
+                    red_l[warp * RU + g] = l_run;
+                    if constexpr (R16) {
+                        red_m[warp * RU + g + 8] = m_run1;
+                        red_l[warp * RU + g + 8] = l_run1;
+                    }
                 }
             }
         }
@@ -571,13 +644,24 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 // the combine buffer aliases the rings: written after the barrier
 #pragma unroll
                 for (int nt = 0; nt < D / 8; ++nt) {
-                    float* dst = red_o + (warp * 8 + g) * D + nt * 8 + 2 * t4;
-                    dst[0] = o[nt][0] + o[nt][2];
-                    dst[1] = o[nt][1] + o[nt][3];
+                    float* dst = red_o + (warp * RU + g) * D + nt * 8 + 2 * t4;
+                    if constexpr (R16) {
+                        dst[0] = o[nt][0];
+                        dst[1] = o[nt][1];
+                        dst[8 * D] = o[nt][2];           // row g + 8
+                        dst[8 * D + 1] = o[nt][3];
+                    } else {
+                        dst[0] = o[nt][0] + o[nt][2];
+                        dst[1] = o[nt][1] + o[nt][3];
+                    }
                 }
                 if (t4 == 0) {
-                    red_m[warp * 8 + g] = m_run;
-                    red_l[warp * 8 + g] = l_run;
+                    red_m[warp * RU + g] = m_run;
+                    red_l[warp * RU + g] = l_run;
+                    if constexpr (R16) {
+                        red_m[warp * RU + g + 8] = m_run1;
+                        red_l[warp * RU + g + 8] = l_run1;
+                    }
                 }
                 fence_proxy_async_smem();   // these generic writes precede later TMA writes here
                 __syncthreads();
@@ -598,16 +682,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const int hh = idx / D, dd = idx - hh * D;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * 8 + hh]);
+                for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * RU + hh]);
                 // M = -inf: no key of this partition is visible to the row (a
                 // later query's keys only); it contributes l = 0, acc = 0
                 const float M_use = (MQ && M == -INFINITY) ? 0.f : M;
                 float lsum = 0.f, acc = 0.f;
 #pragma unroll
                 for (int w = 0; w < kDecWarps; ++w) {
-                    const float f = exp2f(red_m[w * 8 + hh] - M_use);
-                    lsum += f * red_l[w * 8 + hh];
-                    acc += f * red_o[(w * 8 + hh) * D + dd];
+                    const float f = exp2f(red_m[w * RU + hh] - M_use);
+                    lsum += f * red_l[w * RU + hh];
+                    acc += f * red_o[(w * RU + hh) * D + dd];
                 }
                 acc *= v_scale;                                    // 1 unless the pool is FP8
                 const int64_t sh = MQ ? s_rowoff[hh] : static_cast<int64_t>(s) * n_q + h0 + r0 + hh;
@@ -650,14 +734,14 @@ inline int decode_sm_count()
     return cache[dev];
 }
 
-template <typename T, typename QT, int D, int BS, bool FP8, bool MQ>
+template <typename T, typename QT, int D, int BS, bool FP8, bool MQ, int RU = 8>
 cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
 {
     // FP8 runs 3 CTAs per SM (registers capped at 168 by the launch bounds):
     // Llama-3-8B batch 0.273 -> 0.231 ms against 2 CTAs with 24 KB rings.
-    constexpr int NS = decode_stages<T, D, FP8>();
-    using Cfg = DecodeCfg<T, D, NS, FP8>;
-    auto kern = decode_mma_kernel<T, QT, D, BS, NS, FP8, MQ>;
+    constexpr int NS = decode_stages<T, D, FP8, RU>();
+    using Cfg = DecodeCfg<T, D, NS, FP8, RU>;
+    auto kern = decode_mma_kernel<T, QT, D, BS, NS, FP8, MQ, RU>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int per_sm = 1;
@@ -688,7 +772,7 @@ cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
     }
     const int group = a.n_q / a.cache.n_kv_heads;
     const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.max_parts * a.cache.n_kv_heads *
-                          ((group * a.q_per_seq + 7) / 8);
+                          ((group * a.q_per_seq + RU - 1) / RU);
     const int64_t resident = static_cast<int64_t>(decode_sm_count()) * per_sm;
     const unsigned grid = static_cast<unsigned>(upper < resident ? upper : resident);
     kern<<<grid, kDecWarps * 32, Cfg::kDynBytes, s>>>(
@@ -705,6 +789,17 @@ template <typename T, bool MQ>
 cudaError_t run_mma_tc(const DecodeArgs& a, cudaStream_t s, float sl2)
 {
     const int D = a.cache.head_dim, BS = a.cache.block_size;
+    if constexpr (MQ) {
+        // more than 8 (head, query) rows per KV head: 16-row units, so each K/V
+        // stage is read and widened once for all of them
+        if (a.q_per_seq * (a.n_q / a.cache.n_kv_heads) > 8) {
+            if (D == 64 && BS == 16) return run_mma<T, T, 64, 16, false, MQ, 16>(a, s, sl2);
+            if (D == 64 && BS == 32) return run_mma<T, T, 64, 32, false, MQ, 16>(a, s, sl2);
+            if (D == 128 && BS == 16) return run_mma<T, T, 128, 16, false, MQ, 16>(a, s, sl2);
+            if (D == 128 && BS == 32) return run_mma<T, T, 128, 32, false, MQ, 16>(a, s, sl2);
+            return cudaErrorNotSupported;
+        }
+    }
     if (D == 64 && BS == 16) return run_mma<T, T, 64, 16, false, MQ>(a, s, sl2);
     if (D == 64 && BS == 32) return run_mma<T, T, 64, 32, false, MQ>(a, s, sl2);
     if (D == 128 && BS == 16) return run_mma<T, T, 128, 16, false, MQ>(a, s, sl2);
