@@ -175,23 +175,39 @@ class PagedStep:
 
     # ------------------------------------------------------------------
     def step(self, stream=None, prefill_events=None):
-        """One pass of the hot path; all work is enqueued on `stream`.
+        """One pass of the hot path on `stream` (default: the current stream).
         prefill_events: optional (start, stop) torch.cuda.Event pair recorded
-        around the chunked-prefill kernel."""
+        around the chunked-prefill kernel.
+
+        With prefill requests the chunked prefill is launched first, on a side
+        stream, and the decode after it on `stream`: the prefill grid's last
+        wave leaves SMs idle, and the persistent decode's CTAs start on them
+        while it drains.  Both wait for the cache write; `stream` waits for
+        the prefill before the step ends."""
         wl = self.wl
-        self._write(self.new_k, self.new_v, self.new_slots, stream=stream)
-        decode = pa.pa_decode if wl.q_per_seq == 1 else pa.pa_decode_verify
-        decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
-               self.context_lens, wl.scale, wl.block_size, self.workspace, stream=stream,
-               **self.kv_scales)
+        main = stream or torch.cuda.current_stream(self.device)
+        self._write(self.new_k, self.new_v, self.new_slots, stream=main)
         if self.R:
+            side = self._side_stream()
+            side.wait_stream(main)                    # after the cache write
             if prefill_events is not None:
-                prefill_events[0].record(stream or torch.cuda.current_stream())
+                prefill_events[0].record(side)
             pa.pa_prefill_chunk(self.p_out, self.p_q_dev, self.k_cache, self.v_cache,
                                 self.p_block_tables, self.query_start_loc, self.p_context_lens,
-                                int(self.p_chunk.max()), wl.scale, wl.block_size, stream=stream)
+                                int(self.p_chunk.max()), wl.scale, wl.block_size, stream=side)
             if prefill_events is not None:
-                prefill_events[1].record(stream or torch.cuda.current_stream())
+                prefill_events[1].record(side)
+        decode = pa.pa_decode if wl.q_per_seq == 1 else pa.pa_decode_verify
+        decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+               self.context_lens, wl.scale, wl.block_size, self.workspace, stream=main,
+               **self.kv_scales)
+        if self.R:
+            main.wait_stream(side)
+
+    def _side_stream(self):
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(device=self.device)
+        return self._side
 
     # ------------------------------------------------------------------ accounting
     def kv_bytes_unique(self) -> int:
