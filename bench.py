@@ -42,11 +42,11 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # one-pass ncu captures (--metrics dram__bytes_read.sum,dram__bytes_write.sum,
     # full-size workload, 4th launch); profiles/decode_dram_full_size.md
-    ("llama3-8b-bf16", 256, "1a7a48696a67773b"): 2372081152 + 13510144,
-    ("llama3-8b-fp8", 256, "1a7a48696a67773b"): 1188188416 + 12797952,
-    ("llama3-8b-bf16-verify4", 256, "1a7a48696a67773b"): 2386673408 + 45770240,
-    ("opt13b-fp16", 128, "1a7a48696a67773b"): 5371655680 + 8446464,
-    ("mixed-llama3-8b-bf16", 192, "1a7a48696a67773b"): 1446115840 + 9917952,
+    ("llama3-8b-bf16", 256, "11b1d9fb3bd90d93"): 2372039680 + 13611008,
+    ("llama3-8b-fp8", 256, "11b1d9fb3bd90d93"): 1188236800 + 14838528,
+    ("llama3-8b-bf16-verify4", 256, "11b1d9fb3bd90d93"): 2384865792 + 44803584,
+    ("opt13b-fp16", 128, "11b1d9fb3bd90d93"): 5371731200 + 8830208,
+    ("mixed-llama3-8b-bf16", 192, "11b1d9fb3bd90d93"): 1446302720 + 9990912,
 }
 
 
