@@ -174,10 +174,21 @@ class PagedStep:
             pa.pa_reshape_and_cache(k, v, self.k_cache, self.v_cache, slots, stream=stream)
 
     # ------------------------------------------------------------------
-    def step(self, stream=None, prefill_events=None):
+    # per-step inputs and outputs, replaceable by another set (see io_set)
+    IO_NAMES = ("q", "new_k", "new_v", "new_slots", "block_tables", "context_lens", "out",
+                "p_q_dev", "query_start_loc", "p_block_tables", "p_context_lens", "p_out")
+
+    def io_set(self, clone: bool = False) -> dict:
+        """The step's per-step device tensors by name (this object's own, or
+        fresh copies of them, e.g. to double-buffer host uploads)."""
+        io = {n: getattr(self, n) for n in self.IO_NAMES if hasattr(self, n)}
+        return {n: t.clone() for n, t in io.items()} if clone else io
+
+    def step(self, stream=None, prefill_events=None, io=None):
         """One pass of the hot path on `stream` (default: the current stream).
         prefill_events: optional (start, stop) torch.cuda.Event pair recorded
-        around the chunked-prefill kernel.
+        around the chunked-prefill kernel.  io: per-step tensors to use instead
+        of this object's own (same names and shapes as io_set()).
 
         With prefill requests the chunked prefill is launched first, on a side
         stream, and the decode after it on `stream`: the prefill grid's last
@@ -185,21 +196,22 @@ class PagedStep:
         while it drains.  Both wait for the cache write; `stream` waits for
         the prefill before the step ends."""
         wl = self.wl
+        t = self.io_set() if io is None else io
         main = stream or torch.cuda.current_stream(self.device)
-        self._write(self.new_k, self.new_v, self.new_slots, stream=main)
+        self._write(t["new_k"], t["new_v"], t["new_slots"], stream=main)
         if self.R:
             side = self._side_stream()
             side.wait_stream(main)                    # after the cache write
             if prefill_events is not None:
                 prefill_events[0].record(side)
-            pa.pa_prefill_chunk(self.p_out, self.p_q_dev, self.k_cache, self.v_cache,
-                                self.p_block_tables, self.query_start_loc, self.p_context_lens,
+            pa.pa_prefill_chunk(t["p_out"], t["p_q_dev"], self.k_cache, self.v_cache,
+                                t["p_block_tables"], t["query_start_loc"], t["p_context_lens"],
                                 int(self.p_chunk.max()), wl.scale, wl.block_size, stream=side)
             if prefill_events is not None:
                 prefill_events[1].record(side)
         decode = pa.pa_decode if wl.q_per_seq == 1 else pa.pa_decode_verify
-        decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
-               self.context_lens, wl.scale, wl.block_size, self.workspace, stream=main,
+        decode(t["out"], t["q"], self.k_cache, self.v_cache, t["block_tables"],
+               t["context_lens"], wl.scale, wl.block_size, self.workspace, stream=main,
                **self.kv_scales)
         if self.R:
             main.wait_stream(side)
