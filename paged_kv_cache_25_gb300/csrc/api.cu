@@ -110,11 +110,13 @@ int decode_partition_tokens(int64_t seq_groups, int block_size, int max_context_
     // 1024 tokens (64 or 32 blocks) per partition spreads the fixed cost of a
     // unit (block ids, q fragments, the first TMA round trip, the cross-warp
     // combine) over 16 stages per warp and keeps the split-K bytes below 1 %;
-    // halve it (down to 128) while the batch would offer fewer than ~8 units
-    // of work per resident CTA (2 per SM on 152 SMs).
+    // halve it (down to 128) while the batch would offer fewer than ~2 units
+    // of work per resident CTA (2 per SM on 152 SMs): the work counter and the
+    // next-unit prefetch balance the rest (a 64-sequence TinyLlama-shaped
+    // batch: 32.6 us at a bound of 8 units per CTA, 27.0 us at 2).
     int p = 1024;
     while (p > 128 && p > block_size &&
-           seq_groups * ((max_context_len + p - 1) / p) < 2432)
+           seq_groups * ((max_context_len + p - 1) / p) < 608)
         p /= 2;
     return p;
 }
