@@ -266,6 +266,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         x.nchunk = (tok1 - x.tok0 + kRows - 1) / kRows;
         x.blk0 = x.tok0 / BS;
         x.nparts = min((x.L + part_tokens - 1) / part_tokens, max_parts);
+        // without the prefix sums (very large batches) the full-partition
+        // numbering covers every partition index below max_parts - 1: a
+        // sequence's own last partition there belongs to the second numbering
+        if (!use_prefix && gp < n_full && x.part >= x.nparts - 1) x.live = false;
         return x;
     };
     // block id i of unit x (-1 if the table has no such entry), checked

@@ -132,6 +132,23 @@ def test_decode_1024_token_partitions_all_outputs():
     assert err <= TOL[torch.bfloat16], err
 
 
+def test_decode_more_sequences_than_the_prefix_table():
+    """2,100 sequences (past the 2,048 whose partition prefix sums fit in shared
+    memory): units are numbered per (sequence, partition index) instead; every
+    output checked, lengths spanning one to several partitions."""
+    rng = np.random.default_rng(55)
+    lens = [int(x) for x in rng.integers(1, 3001, size=2100)]
+    lens[:7] = [1, 1023, 1024, 1025, 2048, 2049, 3000]
+    wl = _small(56, 2100, 8, 2, 64, 16, torch.bfloat16, lens)
+    st = PagedStep(wl, out_dtype=torch.float32)
+    st.step()
+    torch.cuda.synchronize()
+    _check_clean()
+    ref = oracle_decode(st)
+    err = max_err(st.out, ref)
+    assert err <= TOL[torch.bfloat16], err
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_decode_low_precision_output(dtype):
     wl = _small(21, 4, 32, 8, 128, 16, dtype, [20, 300, 1024, 3000])
