@@ -87,6 +87,7 @@ CASES = [
     (4, 3, 12, 4, 128, 16, torch.bfloat16, [5, 131, 1000], 5),            # g 3 x 5 = 15 rows
     (5, 2, 32, 8, 128, 32, torch.bfloat16, [16, 4096], 16),               # 16 drafts: 8 sub-groups
     (6, 4, 4, 1, 64, 16, torch.float16, [1, 3, 258, 1029], 1),            # one row: plain decode
+    (7, 3, 16, 2, 64, 32, torch.float16, [12, 300, 1500], 3),             # 24 rows: 16 + 8, d 64
 ]
 
 
