@@ -249,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    if rank == 0 or not os.path.exists(pa_build.LIB):
+    if rank == 0:                    # one builder; the other ranks load its library
         pa_build.build()
     if world > 1:
         import torch.distributed as dist
