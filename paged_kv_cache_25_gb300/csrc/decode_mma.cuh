@@ -410,6 +410,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const uint32_t kbase = ring + st * Cfg::kStageBytes;
                 const uint32_t vbase = kbase + Cfg::kSlabBytes;
                 float sc[2][4];
+                float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 
                 if constexpr (FP8) {
                     if (valid < kRows) {
@@ -448,9 +449,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                                 const uint32_t a[4] = {qa[kk][0], 0u, qa[kk][1], 0u};
                                 uint32_t b0, b1;
                                 e4m3x4_to_h2x2(w[jj], b0, b1);
-                                MmaOp<T>::run(sc[nt], a, b0, b1);
+                                // two accumulator chains (even / odd 16 columns) halve the
+                                // dependent MMA sequence per n-tile
+                                MmaOp<T>::run((jj & 1) ? sc2[nt] : sc[nt], a, b0, b1);
                             }
                         }
+                        sc[nt][0] += sc2[nt][0]; sc[nt][1] += sc2[nt][1];
+                        sc[nt][2] += sc2[nt][2]; sc[nt][3] += sc2[nt][3];
                     }
                 } else {
                     if (valid < kRows) {
