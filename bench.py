@@ -42,11 +42,11 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # one-pass ncu captures (--metrics dram__bytes_read.sum,dram__bytes_write.sum,
     # full-size workload, 4th launch); profiles/decode_dram_full_size.md
-    ("llama3-8b-bf16", 256, "11b1d9fb3bd90d93"): 2372039680 + 13611008,
-    ("llama3-8b-fp8", 256, "11b1d9fb3bd90d93"): 1188236800 + 14838528,
-    ("llama3-8b-bf16-verify4", 256, "11b1d9fb3bd90d93"): 2384865792 + 44803584,
-    ("opt13b-fp16", 128, "11b1d9fb3bd90d93"): 5371731200 + 8830208,
-    ("mixed-llama3-8b-bf16", 192, "11b1d9fb3bd90d93"): 1446302720 + 9990912,
+    ("llama3-8b-bf16", 256, "ad80b383e235384f"): 2371977216 + 13616640,
+    ("llama3-8b-fp8", 256, "ad80b383e235384f"): 1188184576 + 12948224,
+    ("llama3-8b-bf16-verify4", 256, "ad80b383e235384f"): 2384849152 + 44538624,
+    ("opt13b-fp16", 128, "ad80b383e235384f"): 5371655936 + 8389376,
+    ("mixed-llama3-8b-bf16", 192, "ad80b383e235384f"): 1446247936 + 9858304,
 }
 
 
