@@ -210,14 +210,18 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
  * (pa_reshape_and_cache).  With no earlier context it is ordinary causal
  * prefill of the whole prompt.
  *   out, q          : [total_q][n_q_heads][head_dim], request r's rows start at
- *                     query_start_loc[r]; out in out_dtype, q in cache dtype.
+ *                     query_start_loc[r]; out in out_dtype, q in the cache
+ *                     dtype (FP8 pools: in cache->act_dtype).
  *   query_start_loc : int32 [num_reqs + 1] on the device, non-decreasing,
  *                     query_start_loc[0] = 0; C_r = difference of neighbours.
  *   context_lens    : int32 [num_reqs] on the device: total tokens L_r of
  *                     request r including the chunk (C_r <= L_r).
  *   max_query_len   : host value >= every C_r (sizes the grid).
  *   workspace       : reserved; pass NULL / 0 (pa_prefill_workspace_size is 0).
- * bf16 and fp16 pools only (FP8 pools return PA_ERR_UNSUPPORTED). */
+ * bf16, fp16 and FP8 E4M3 pools (f32 pools return PA_ERR_UNSUPPORTED).  FP8
+ * pools keep V transposed per block as for decode; their codes are widened
+ * exactly to act_dtype on chip and the scales are folded into the softmax
+ * scale (k_scale) and the output (v_scale). */
 pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q,
                            const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
                            const int32_t* block_tables, int max_blocks_per_seq,

@@ -238,11 +238,12 @@ def pa_prefill_workspace_size(num_reqs, n_q_heads, head_dim, total_q) -> int:
 
 def pa_prefill_chunk(out, q, k_cache, v_cache, block_tables, query_start_loc, context_lens,
                      max_query_len: int, scale: float, block_size: int, workspace=None,
-                     stream=None):
-    """Chunked prefill: out/q [sum C][n_q][d]; query_start_loc int32 [R+1]."""
+                     stream=None, k_scale=None, v_scale=None):
+    """Chunked prefill: out/q [sum C][n_q][d]; query_start_loc int32 [R+1].
+    FP8 pools also take k_scale and v_scale."""
     R = int(context_lens.shape[0])
     n_q = int(q.shape[1])
-    d = _desc(k_cache)
+    d = _desc(k_cache, k_scale, v_scale, q.dtype)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().pa_prefill_chunk(_ptr(out), dtype_code(out.dtype), _ptr(q), _ptr(k_cache),
                                   _ptr(v_cache), C.byref(d), _ptr(block_tables),

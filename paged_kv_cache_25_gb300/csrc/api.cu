@@ -460,8 +460,8 @@ pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q, const v
     if (st != PA_OK) return st;
     if (num_reqs < 0 || max_query_len < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
     if (num_reqs == 0 || max_query_len == 0) return ok();
-    if (cache->dtype == PA_F32 || cache->dtype == PA_FP8_E4M3)
-        return fail(PA_ERR_UNSUPPORTED, "chunked prefill runs on bf16/fp16 pools only");
+    if (cache->dtype == PA_F32)
+        return fail(PA_ERR_UNSUPPORTED, "chunked prefill runs on bf16/fp16/FP8 pools only");
     if (cache->head_dim != 64 && cache->head_dim != 128)
         return fail(PA_ERR_UNSUPPORTED, "chunked prefill supports head_dim 64 and 128");
     if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16)

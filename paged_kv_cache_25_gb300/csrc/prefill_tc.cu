@@ -27,7 +27,14 @@
 //             and writes P back over its scores in TMEM as hi + lo bf16/fp16
 //             halves (P V keeps ~16 bits of P); the P V MMA takes P straight
 //             from TMEM.  At the end O / l goes to global memory.
+// FP8 (E4M3) pools: the producer warps TMA each key tile's codes into a
+// staging buffer and widen them (exactly) into the same K ring; V is kept in
+// the pool's transposed [d][keys] order and widened into a K-major operand of
+// P V.  Keys at or past the context are written as zeros.  k_scale is folded
+// into the softmax scale and v_scale into the output.
 // All waits are bounded; the kernel never traps.
+#include <cuda_fp8.h>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -47,15 +54,18 @@ constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1, kMmaWarp = kSo
 constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;   // softmax, K producer, V producer, MMA
 constexpr uint32_t kTmemCols = 512;   // S/P_A [0,128) S/P_B [128,256) O_A, O_B from 256
 
-template <typename T, int D>
+template <typename T, int D, bool F8 = false>
 struct PfLayout {
     static constexpr int kHalves = D / 64;
     static constexpr uint32_t kQBytes = kTcRows * D * 2;          // one Q tile
     static constexpr uint32_t kKBytes = kTcKeys * D * 2;          // K (or V) of one key tile
+    static constexpr uint32_t kCodeBytes = kTcKeys / 2 * D;       // FP8: codes of half a key tile
     static constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
     static constexpr uint32_t kOffK = kOffQ + kTcTiles * kQBytes; // K ring
     static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
-    static constexpr uint32_t kDynBytes = kOffV + kTcStages * kKBytes + 1024;
+    static constexpr uint32_t kOffKS = kOffV + kTcStages * kKBytes;  // FP8: K codes staging
+    static constexpr uint32_t kOffVS = kOffKS + (F8 ? kCodeBytes : 0);   // FP8: V codes staging
+    static constexpr uint32_t kDynBytes = kOffVS + (F8 ? kCodeBytes : 0) + 1024;
     // S_t at t * 128; P_t overwrites it, keys 32c .. 32c+31 as hi in columns
     // 32c .. 32c+15 and lo in 32c+16 .. 32c+31 (two 16-bit values per column)
     static constexpr uint32_t kTmemS = 0;
@@ -95,18 +105,48 @@ __device__ __forceinline__ void store_row(void* out, int64_t base, int col, cons
     }
 }
 
-template <typename T, int D, int BS>
+// Four E4M3 codes -> four T values (exact), as two packed pairs.
+template <typename T>
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi)
+{
+    __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
+    __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+    if constexpr (std::is_same<T, __half>::value) {
+        lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
+        hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+    } else {
+        lo = Cvt<__nv_bfloat16>::pack(__half2float(__ushort_as_half(a.x)), __half2float(__ushort_as_half(a.y)));
+        hi = Cvt<__nv_bfloat16>::pack(__half2float(__ushort_as_half(b.x)), __half2float(__ushort_as_half(b.y)));
+    }
+}
+
+// Sixteen codes of k-order positions i (low byte first) with the ones at or
+// past `keep` replaced by zeros.
+__device__ __forceinline__ uint4 keep_codes(uint4 c, int keep)
+{
+    uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int k = min(4, max(0, keep - 4 * e));
+        w[e] &= k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T, int D, int BS, bool F8 = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   void* __restrict__ out, pa_dtype out_dtype, const T* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
                   const int32_t* __restrict__ q_start, const int32_t* __restrict__ context_lens,
-                  int n_q, int n_kv, int group, int num_blocks, float scale_log2, unsigned* err)
+                  int n_q, int n_kv, int group, int num_blocks, float scale_log2, float v_scale,
+                  unsigned* err)
 {
-    using Ly = PfLayout<T, D>;
+    using Ly = PfLayout<T, D, F8>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdescQK = idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
-    constexpr uint32_t kIdescPV = idesc_f16(kBf16, false, true, kTcRows, D);
+    // P V: V as [keys][d] (MN-major) from 16-bit pools, as [d][keys] (K-major) from FP8
+    constexpr uint32_t kIdescPV = idesc_f16(kBf16, false, !F8, kTcRows, D);
     static_assert(BS % 16 == 0 && kTcKeys % BS == 0, "block size must divide the key tile");
 
     // blocks with more keys first: the last position blocks are the heaviest
@@ -139,6 +179,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages];
     __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
     __shared__ __align__(8) uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles], q_ready;
+    __shared__ __align__(8) uint64_t code_full[2];   // FP8: K / V codes of a key tile landed
     __shared__ uint32_t s_tmem;
     // partial row maxima of the two threads of a row (double-buffered by key
     // tile), a "stop" flag beside each, and the partial row sums at the end
@@ -165,6 +206,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mbar_init(smem_u32(&pv_done[t]), 1);
         }
         mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
+        mbar_init(smem_u32(&code_full[0]), 1);
+        mbar_init(smem_u32(&code_full[1]), 1);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
@@ -176,7 +219,105 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp == kKWarp || warp == kVWarp) {
+    if ((warp == kKWarp || warp == kVWarp) && F8) {
+        // ------------------------------------------------ FP8 producers
+        // A key tile's codes come in two halves of 64 keys: lane 0 brings one
+        // into the staging buffer, the warp widens it into the ring stage and
+        // lane 0 requests the next half as soon as the buffer has been read.
+        const bool is_k = warp == kKWarp;
+        const CUtensorMap* map = is_k ? &kmap : &vmap;
+        uint64_t* full_bar = is_k ? k_full : v_full;
+        uint64_t* empty_bar = is_k ? k_empty : v_empty;
+        const uint32_t ring_base = sbase + (is_k ? Ly::kOffK : Ly::kOffV);
+        const uint32_t stage = sbase + (is_k ? Ly::kOffKS : Ly::kOffVS);
+        const uint32_t cbar = smem_u32(&code_full[is_k ? 0 : 1]);
+        const uint8_t* stage_ptr = smem + (is_k ? Ly::kOffKS : Ly::kOffVS);
+        constexpr int kHalfKeys = kTcKeys / 2;
+        auto request = [&](int j, int h) {
+            mbar_arrive_expect_tx(cbar, Ly::kCodeBytes);
+            int b = 0;
+#pragma unroll
+            for (int c = 0; c < kHalfKeys / 16; ++c) {
+                const int key0 = j * kTcKeys + h * kHalfKeys + c * 16;
+                if (key0 < L) {   // past L the codes are replaced by zeros: reuse the last block
+                    const int lb = key0 / BS;
+                    b = lb < max_blocks ? __ldg(block_tables + static_cast<int64_t>(r) * max_blocks + lb) : -1;
+                    if (b < 0 || b >= num_blocks) {
+                        set_error(err, PA_ERR_OUT_OF_RANGE);
+                        b = 0;
+                    }
+                }
+                if (is_k)   // 16 rows of D codes
+                    tma_load_2d(stage + c * 16 * D, map, 0, (b * n_kv + kvh) * BS + key0 % BS, cbar);
+                else        // D rows of 16 codes (the pool's transposed slab)
+                    tma_load_2d(stage + c * 16 * D, map, key0 % BS, (b * n_kv + kvh) * D, cbar);
+            }
+        };
+        if (lane == 0) {
+            prefetch_tensormap(map);
+            if (n_tiles > 0) request(0, 0);   // a tile's first key is always below L
+        }
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j % kTcStages;
+            bool ok = true;
+            if (j >= kTcStages) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(smem_u32(&empty_bar[st]), ((j / kTcStages) - 1) & 1, err));
+                if (!ok) mbar_wait(cbar, 0, err);   // half 0 of this tile is in flight
+            }
+            const int keep_tile = L - j * kTcKeys;        // valid keys of this tile (may exceed 128)
+            const uint32_t dst = ring_base + st * Ly::kKBytes;
+#pragma unroll 1
+            for (int h = 0; h < 2 && ok; ++h) {
+                // completion 2j + h of the staging barrier
+                const bool landed = mbar_wait(cbar, h, err);
+                if (!__all_sync(0xffffffffu, landed)) {
+                    // the wait ran out (error recorded): let the copy land (bounded)
+                    // before the CTA can exit
+                    mbar_wait(cbar, h, err);
+                    ok = false;
+                    break;
+                }
+                // 64 x D codes: unit u = 16 codes of one K row (or of one V^T
+                // row's 16-key chunk); each becomes two 16-byte ring chunks
+                for (int u = lane; u < kHalfKeys * D / 16; u += 32) {
+                    uint4 c = *reinterpret_cast<const uint4*>(stage_ptr + u * 16);
+                    uint32_t w[8];
+                    int row, chunk0;   // ring row and first 8-element chunk
+                    if (is_k) {
+                        row = h * kHalfKeys + u / (D / 16);       // key in the tile
+                        chunk0 = 2 * (u % (D / 16));              // d chunk
+                        if (row >= keep_tile) c = make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+                        const int cc = h * (kHalfKeys / 16) + u / D;   // 16-key chunk
+                        row = u % D;                                   // d
+                        chunk0 = 2 * cc;                               // key chunk (8 keys)
+                        c = keep_codes(c, keep_tile - 16 * cc);
+                    }
+                    widen4<T>(c.x, w[0], w[1]);
+                    widen4<T>(c.y, w[2], w[3]);
+                    widen4<T>(c.z, w[4], w[5]);
+                    widen4<T>(c.w, w[6], w[7]);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int ch = chunk0 + e;
+                        // K: [keys][d] in 64-column halves; V: [d][keys] in 64-key halves
+                        const uint32_t addr = dst + (ch >> 3) * ((is_k ? kTcKeys : D) * 128) +
+                                              row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+                        st_shared_v4(addr, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    }
+                }
+                fence_proxy_async_smem();   // ring writes -> MMA reads; staging reads -> next TMA
+                __syncwarp();
+                if (lane == 0) {
+                    if (h == 0) request(j, 1);
+                    else if (j + 1 < n_tiles) request(j + 1, 0);
+                }
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) mbar_arrive(smem_u32(&full_bar[st]));
+        }
+    } else if (warp == kKWarp || warp == kVWarp) {
         // ------------------------------------------------ TMA producers
         // K and V have separate rings: K of key tile j is released once both
         // S_t(j) are done, V of tile j once both P_t(j) V are.
@@ -221,7 +362,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (lane == 0) {
             const uint64_t dq = sdesc_sw128(sbase + Ly::kOffQ, 16, 1024);
             const uint64_t dk = sdesc_sw128(sbase + Ly::kOffK, 16, 1024);
-            const uint64_t dv = sdesc_sw128(sbase + Ly::kOffV, kTcKeys * 128, 1024);
+            // V: MN-major [keys][d] halves (16-bit pools) or K-major [d][keys] halves (FP8)
+            const uint64_t dv = F8 ? sdesc_sw128(sbase + Ly::kOffV, 16, 1024)
+                                   : sdesc_sw128(sbase + Ly::kOffV, kTcKeys * 128, 1024);
             constexpr uint32_t kQHalf = (kTcRows * 128) >> 4, kKHalf = (kTcKeys * 128) >> 4;
             constexpr uint32_t kKStage = Ly::kKBytes >> 4, kQTile = Ly::kQBytes >> 4;
             // S_t(j) = Q_t K_j^T; the K stage is released after the last tile's
@@ -249,9 +392,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     // keys 16 ks .. +15: 32-key chunk ks / 2 holds hi in its first
                     // 16 columns and lo in the next 16 (16 keys = 8 columns)
                     const uint32_t col = (ks >> 1) * 32 + (ks & 1) * 8;
-                    umma_f16_ts(d_o, a_p + col, dvs + ks * (2048 >> 4), kIdescPV,
-                                (j > 0 || ks > 0) ? 1u : 0u);
-                    umma_f16_ts(d_o, a_p + col + 16, dvs + ks * (2048 >> 4), kIdescPV, 1u);
+                    // V rows of these 16 keys: 16 rows of 128 B (MN-major), or
+                    // 32 B into a 64-key half of the [d][keys] tile (K-major)
+                    const uint32_t vst = F8 ? (ks >> 2) * ((D * 128) >> 4) + (ks & 3) * 2
+                                            : ks * (2048 >> 4);
+                    umma_f16_ts(d_o, a_p + col, dvs + vst, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16_ts(d_o, a_p + col + 16, dvs + vst, kIdescPV, 1u);
                 }
                 umma_commit(smem_u32(&pv_done[t]));
             };
@@ -430,7 +576,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             tmem_st_wait();
 
-            if (key0 + kTcKeys > L) {
+            if (!F8 && key0 + kTcKeys > L) {   // FP8: the producers wrote zeros there
                 // keys at or past L (only in the request's last key tile) may hold
                 // anything, even NaN: zero those V rows so P = 0 keeps them out,
                 // after the tile's V has landed.  Both tiles' rows may do this for
@@ -468,7 +614,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                             mbar_wait(smem_u32(&pv_done[t]), (nt - 1) & 1, err);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
-                const float inv = 1.f / lsum;
+                const float inv = (F8 ? v_scale : 1.f) / lsum;
                 const int64_t obase = (static_cast<int64_t>(qs + pos_local) * n_q + head) * D;
 #pragma unroll
                 for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -490,11 +636,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool F8>
 static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl2)
 {
-    using Ly = PfLayout<T, D>;
-    auto kern = prefill_tc_kernel<T, D, BS>;
+    using Ly = PfLayout<T, D, F8>;
+    auto kern = prefill_tc_kernel<T, D, BS, F8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -504,35 +650,48 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap kmap, vmap;
     const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
-    if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK ||
-        encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK)
-        return cudaErrorInvalidValue;
+    if constexpr (F8) {
+        // codes without swizzle: K boxes of 16 rows x D codes; V^T boxes of D
+        // rows x 16 codes of the transposed [d][block_size] slabs
+        const uint64_t vrows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * D;
+        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, D, 16, 0) != PA_OK ||
+            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, BS, vrows, 16, D, 0) != PA_OK)
+            return cudaErrorInvalidValue;
+    } else {
+        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK ||
+            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK)
+            return cudaErrorInvalidValue;
+    }
     const int group = a.n_q / a.cache.n_kv_heads;
     const int64_t tiles = (static_cast<int64_t>(a.max_q) * group + kTcTiles * kTcRows - 1) /
                           (kTcTiles * kTcRows);
     dim3 grid(static_cast<unsigned>(tiles), a.cache.n_kv_heads, a.num_reqs);
     kern<<<grid, kTcThreads, Ly::kDynBytes, s>>>(
         kmap, vmap, a.out, a.out_dtype, static_cast<const T*>(a.q), a.block_tables, a.max_blocks,
-        a.q_start, a.context_lens, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks, sl2, a.err);
+        a.q_start, a.context_lens, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
+        F8 ? sl2 * a.cache.k_scale : sl2, F8 ? a.cache.v_scale : 1.f, a.err);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool F8>
 static cudaError_t run_prefill_tc_dt(const PrefillArgs& a, cudaStream_t s, float sl2)
 {
     const int D = a.cache.head_dim, BS = a.cache.block_size;
-    if (D == 64 && BS == 16) return run_prefill_tc<T, 64, 16>(a, s, sl2);
-    if (D == 64 && BS == 32) return run_prefill_tc<T, 64, 32>(a, s, sl2);
-    if (D == 128 && BS == 16) return run_prefill_tc<T, 128, 16>(a, s, sl2);
-    if (D == 128 && BS == 32) return run_prefill_tc<T, 128, 32>(a, s, sl2);
+    if (D == 64 && BS == 16) return run_prefill_tc<T, 64, 16, F8>(a, s, sl2);
+    if (D == 64 && BS == 32) return run_prefill_tc<T, 64, 32, F8>(a, s, sl2);
+    if (D == 128 && BS == 16) return run_prefill_tc<T, 128, 16, F8>(a, s, sl2);
+    if (D == 128 && BS == 32) return run_prefill_tc<T, 128, 32, F8>(a, s, sl2);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s)
 {
     const float sl2 = a.scale * 1.4426950408889634f;
-    if (a.cache.dtype == PA_BF16) return run_prefill_tc_dt<__nv_bfloat16>(a, s, sl2);
-    if (a.cache.dtype == PA_F16) return run_prefill_tc_dt<__half>(a, s, sl2);
+    if (a.cache.dtype == PA_BF16) return run_prefill_tc_dt<__nv_bfloat16, false>(a, s, sl2);
+    if (a.cache.dtype == PA_F16) return run_prefill_tc_dt<__half, false>(a, s, sl2);
+    if (a.cache.dtype == PA_FP8_E4M3)   // queries (and the widened K/V) in the activation type
+        return a.cache.act_dtype == PA_BF16 ? run_prefill_tc_dt<__nv_bfloat16, true>(a, s, sl2)
+                                            : run_prefill_tc_dt<__half, true>(a, s, sl2);
     return cudaErrorInvalidValue;
 }
 

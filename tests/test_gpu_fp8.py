@@ -9,7 +9,7 @@ import oracle
 from paged_kv_cache_25_gb300 import binding as pa
 from paged_kv_cache_25_gb300 import inputs
 from paged_kv_cache_25_gb300.step import PagedStep
-from tests.helpers import max_err, oracle_decode
+from tests.helpers import half_ulp, max_err, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -82,13 +82,78 @@ def test_fp8_decode_full_size_sampled():
     assert torch.isfinite(st.out).all()
 
 
-def test_fp8_prefill_is_refused():
+def _fp8_prefill_case(seed, specs, n_q, n_kv, d, bs, act, scale, out_dtype=torch.float32,
+                      v_scale=None):
+    """specs: list of (cached tokens, chunk).  The context and the chunk go
+    through the quantizing cache write; the oracle attends over the codes
+    times the scale (v_scale for V when given)."""
+    vsc = scale if v_scale is None else v_scale
+    rng = np.random.default_rng(seed)
+    R = len(specs)
+    lens = [c + n for c, n in specs]
+    nb = sum(-(-L // bs) for L in lens) + 5
+    alloc = pa.Allocator(nb, rng.permutation(nb).astype(np.int32))
+    mb = max(-(-L // bs) for L in lens)
+    tables = alloc.build_tables(lens, mb, bs)
+    g = torch.Generator().manual_seed(seed)
+    ks = [torch.randn(L, n_kv, d, generator=g).to(act) for L in lens]
+    vs = [torch.randn(L, n_kv, d, generator=g).to(act) for L in lens]
+    qs = [torch.randn(n, n_q, d, generator=g).to(act) for _, n in specs]
+    kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    seq = np.concatenate([np.full(L, r, np.int32) for r, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
+    slots = torch.from_numpy(pa.pa_slot_mapping(tables, bs, seq, pos)).cuda()
+    pa.pa_reshape_and_cache_quant(torch.cat(ks).cuda(), torch.cat(vs).cuda(), kc, vc, slots,
+                                  k_scale=scale, v_scale=vsc)
+    qsl = np.zeros(R + 1, np.int32)
+    qsl[1:] = np.cumsum([n for _, n in specs])
+    out = torch.full((int(qsl[-1]), n_q, d), float("nan"), dtype=out_dtype, device="cuda")
+    pa.pa_prefill_chunk(out, torch.cat(qs).cuda(), kc, vc, torch.from_numpy(tables).cuda(),
+                        torch.from_numpy(qsl).cuda(),
+                        torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                        max(n for _, n in specs), 1.0 / np.sqrt(d), bs,
+                        k_scale=scale, v_scale=vsc)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    kd = [oracle.dequantize_fp8(oracle.quantize_fp8(x, scale), scale) for x in ks]
+    vd = [oracle.dequantize_fp8(oracle.quantize_fp8(x, vsc), vsc) for x in vs]
+    ref = np.concatenate(oracle.prefill(qs, kd, vd, float(np.float32(1.0 / np.sqrt(d)))))
+    return out, ref
+
+
+PREFILL_CASES = [
+    # seed, specs (ctx, chunk), n_q, n_kv, d, bs, act dtype, scale
+    (21, [(0, 37)], 4, 4, 64, 16, torch.bfloat16, 1.0 / 64),                        # plain causal
+    (22, [(0, 200), (100, 1), (33, 47)], 32, 8, 128, 16, torch.bfloat16, 1.0 / 64),  # ragged
+    (23, [(500, 64), (0, 16), (16, 16)], 8, 1, 64, 32, torch.float16, 0.0125),       # MQA, bs 32
+    (24, [(1000, 130)], 8, 8, 128, 32, torch.float16, 0.0125),                       # MHA, tail 106
+    (25, [(47, 200), (1, 3), (300, 129)], 12, 4, 128, 32, torch.bfloat16, 1.0 / 64),  # g=3
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=[f"fp{c[0]}" for c in PREFILL_CASES])
+def test_fp8_prefill_matches_oracle_on_dequantized_kv(case):
+    out, ref = _fp8_prefill_case(*case)
+    assert max_err(out, ref) <= 2e-3
+
+
+def test_fp8_prefill_bf16_output_and_unequal_scales():
+    out, ref = _fp8_prefill_case(26, [(300, 100), (0, 50)], 32, 8, 128, 16, torch.bfloat16,
+                                 1.0 / 64, out_dtype=torch.bfloat16, v_scale=0.0125)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2e-3 + half_ulp(ref, torch.bfloat16))
+
+
+def test_fp8_prefill_needs_scales():
     nb = 4
     kc = torch.zeros((nb, 2, 16, 64), dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.zeros((nb, 2, 64, 16), dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
     out = torch.empty((8, 4, 64), dtype=torch.float32, device="cuda")
-    with pytest.raises(pa.PAError) as e:
-        pa.pa_prefill_chunk(out, torch.zeros((8, 4, 64), dtype=torch.bfloat16, device="cuda"), kc, kc,
+    with pytest.raises(pa.PAError) as e:   # no scales: refused on the host
+        pa.pa_prefill_chunk(out, torch.zeros((8, 4, 64), dtype=torch.bfloat16, device="cuda"), kc, vc,
                             torch.zeros((1, 4), dtype=torch.int32, device="cuda"),
                             torch.tensor([0, 8], dtype=torch.int32, device="cuda"),
                             torch.tensor([8], dtype=torch.int32, device="cuda"), 8, 0.125, 16)
-    assert e.value.status in (pa.PA_ERR_UNSUPPORTED, pa.PA_ERR_INVALID_ARG)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    assert pa.pa_get_device_error() == 0
