@@ -50,8 +50,20 @@ constexpr int kTcTiles = 2;       // tiles per CTA (A, B)
 constexpr int kTcKeys = 128;      // keys per key tile
 constexpr int kTcStages = 2;      // K/V ring depth
 constexpr int kSoftmaxWarps = 8 * kTcTiles;   // two threads per row of each tile
-constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1, kMmaWarp = kSoftmaxWarps + 2;
-constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;   // softmax, K producer, V producer, MMA
+constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1;
+// FP8 pools: warps that widen codes into the rings.  A key tile is 2 x
+// (128 / kF8ChunkKeys) chunks (K's, then V's); chunk g of the whole sequence
+// goes to converter g % kF8Converters.
+constexpr int kF8Converters = 3;
+constexpr int kF8ChunkKeys = 32;   // keys per staged chunk of codes (16 or 32)
+// Warps after the softmax ones: the K and V producers (or FP8 converters),
+// then the MMA issuer.
+template <bool F8>
+struct PfWarps {
+    static constexpr int kProducers = F8 ? kF8Converters : 2;
+    static constexpr int kMma = kSoftmaxWarps + kProducers;
+    static constexpr int kThreads = (kMma + 1) * 32;
+};
 constexpr uint32_t kTmemCols = 512;   // S/P_A [0,128) S/P_B [128,256) O_A, O_B from 256
 
 template <typename T, int D, bool F8 = false>
@@ -59,13 +71,12 @@ struct PfLayout {
     static constexpr int kHalves = D / 64;
     static constexpr uint32_t kQBytes = kTcRows * D * 2;          // one Q tile
     static constexpr uint32_t kKBytes = kTcKeys * D * 2;          // K (or V) of one key tile
-    static constexpr uint32_t kCodeBytes = kTcKeys / 2 * D;       // FP8: codes of half a key tile
+    static constexpr uint32_t kCodeBytes = kF8ChunkKeys * D;      // FP8: codes of one staged chunk
     static constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
     static constexpr uint32_t kOffK = kOffQ + kTcTiles * kQBytes; // K ring
     static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
-    static constexpr uint32_t kOffKS = kOffV + kTcStages * kKBytes;  // FP8: K codes staging
-    static constexpr uint32_t kOffVS = kOffKS + (F8 ? kCodeBytes : 0);   // FP8: V codes staging
-    static constexpr uint32_t kDynBytes = kOffVS + (F8 ? kCodeBytes : 0) + 1024;
+    static constexpr uint32_t kOffCS = kOffV + kTcStages * kKBytes;  // FP8: 2 code buffers per converter
+    static constexpr uint32_t kDynBytes = kOffCS + (F8 ? kF8Converters * 2 * kCodeBytes : 0) + 1024;
     // S_t at t * 128; P_t overwrites it, keys 32c .. 32c+31 as hi in columns
     // 32c .. 32c+15 and lo in 32c+16 .. 32c+31 (two 16-bit values per column)
     static constexpr uint32_t kTmemS = 0;
@@ -105,18 +116,30 @@ __device__ __forceinline__ void store_row(void* out, int64_t base, int col, cons
     }
 }
 
-// Four E4M3 codes -> four T values (exact), as two packed pairs.
+// Four E4M3 codes -> four T values (exact), as two packed pairs.  fp16: the
+// hardware pair conversion.  bf16: the code's sign, exponent and mantissa
+// fields moved into place make a bf16 of value code * 2^-120 (E4M3 bias 7,
+// bf16 bias 127; E4M3 subnormals land on bf16 subnormals), which one exact
+// multiply by 2^120 restores.
 template <typename T>
 __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
-    __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
     if constexpr (std::is_same<T, __half>::value) {
-        lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
-        hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+        asm("{\n\t.reg .b16 a, b;\n\t"
+            "mov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
     } else {
-        lo = Cvt<__nv_bfloat16>::pack(__half2float(__ushort_as_half(a.x)), __half2float(__ushort_as_half(a.y)));
-        hi = Cvt<__nv_bfloat16>::pack(__half2float(__ushort_as_half(b.x)), __half2float(__ushort_as_half(b.y)));
+        const uint32_t x0 = __byte_perm(w, 0u, 0x4140), x1 = __byte_perm(w, 0u, 0x4342);
+        const uint32_t b0 = ((x0 << 4) & 0x07F007F0u) | ((x0 << 8) & 0x80008000u);
+        const uint32_t b1 = ((x1 << 4) & 0x07F007F0u) | ((x1 << 8) & 0x80008000u);
+        // 0x7B80 = 2^120 in bf16; adding -0 keeps the fma a plain exact product
+        asm("fma.rn.bf16x2 %0, %2, %4, %5;\n\t"
+            "fma.rn.bf16x2 %1, %3, %4, %5;"
+            : "=r"(lo), "=r"(hi)
+            : "r"(b0), "r"(b1), "r"(0x7B807B80u), "r"(0x80008000u));
     }
 }
 
@@ -134,7 +157,7 @@ __device__ __forceinline__ uint4 keep_codes(uint4 c, int keep)
 }
 
 template <typename T, int D, int BS, bool F8 = false>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(PfWarps<F8>::kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   void* __restrict__ out, pa_dtype out_dtype, const T* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
@@ -143,6 +166,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                   unsigned* err)
 {
     using Ly = PfLayout<T, D, F8>;
+    constexpr int kMmaWarp = PfWarps<F8>::kMma;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdescQK = idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
     // P V: V as [keys][d] (MN-major) from 16-bit pools, as [d][keys] (K-major) from FP8
@@ -179,14 +203,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages];
     __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
     __shared__ __align__(8) uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles], q_ready;
-    __shared__ __align__(8) uint64_t code_full[2];   // FP8: K / V codes of a key tile landed
+    __shared__ __align__(8) uint64_t code_full[kF8Converters][2];   // FP8: codes landed, per converter and buffer
     __shared__ uint32_t s_tmem;
     // partial row maxima of the two threads of a row (double-buffered by key
     // tile), a "stop" flag beside each, and the partial row sums at the end
     __shared__ float xmax[2][kTcTiles][2][kTcRows];
-    __shared__ int xstop[2][kTcTiles][2][kTcRows];
+    __shared__ uint8_t xstop[2][kTcTiles][2][kTcRows];
     __shared__ float xsum[kTcTiles][2][kTcRows];
-    __shared__ int xstop_end[kTcTiles][2][kTcRows];
+    __shared__ uint8_t xstop_end[kTcTiles][2][kTcRows];
     extern __shared__ uint8_t dyn_smem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -195,9 +219,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < kTcStages; ++i) {
-            mbar_init(smem_u32(&k_full[i]), 1);
+            // FP8: one arrival per widened chunk; 16-bit pools: the TMA's
+            mbar_init(smem_u32(&k_full[i]), F8 ? kTcKeys / kF8ChunkKeys : 1);
             mbar_init(smem_u32(&k_empty[i]), 1);
-            mbar_init(smem_u32(&v_full[i]), 1);
+            mbar_init(smem_u32(&v_full[i]), F8 ? kTcKeys / kF8ChunkKeys : 1);
             mbar_init(smem_u32(&v_empty[i]), 1);
         }
         for (int t = 0; t < kTcTiles; ++t) {
@@ -206,8 +231,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mbar_init(smem_u32(&pv_done[t]), 1);
         }
         mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
-        mbar_init(smem_u32(&code_full[0]), 1);
-        mbar_init(smem_u32(&code_full[1]), 1);
+        for (int i = 0; i < 2 * kF8Converters; ++i) mbar_init(smem_u32(&code_full[i >> 1][i & 1]), 1);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
@@ -219,103 +243,160 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if ((warp == kKWarp || warp == kVWarp) && F8) {
-        // ------------------------------------------------ FP8 producers
-        // A key tile's codes come in two halves of 64 keys: lane 0 brings one
-        // into the staging buffer, the warp widens it into the ring stage and
-        // lane 0 requests the next half as soon as the buffer has been read.
-        const bool is_k = warp == kKWarp;
-        const CUtensorMap* map = is_k ? &kmap : &vmap;
-        uint64_t* full_bar = is_k ? k_full : v_full;
-        uint64_t* empty_bar = is_k ? k_empty : v_empty;
-        const uint32_t ring_base = sbase + (is_k ? Ly::kOffK : Ly::kOffV);
-        const uint32_t stage = sbase + (is_k ? Ly::kOffKS : Ly::kOffVS);
-        const uint32_t cbar = smem_u32(&code_full[is_k ? 0 : 1]);
-        const uint8_t* stage_ptr = smem + (is_k ? Ly::kOffKS : Ly::kOffVS);
-        constexpr int kHalfKeys = kTcKeys / 2;
-        auto request = [&](int j, int h) {
-            mbar_arrive_expect_tx(cbar, Ly::kCodeBytes);
-            int b = 0;
+    if (F8 && warp >= kSoftmaxWarps && warp < kMmaWarp) {
+        // ------------------------------------------------ FP8 converters
+        // Chunk g (tile g / (2 kChunks); K chunks first, then V) is widened by
+        // converter g % kF8Converters into its ring stage, which then gets
+        // one arrival on its full barrier.  Each converter's chunks pass
+        // through two staging buffers: while it widens its chunk n, chunk n + 1
+        // is in flight, and lane 0 requests chunk n + 2 into the same buffer
+        // once the warp has read it.  The block ids of a tile's 16-key pieces
+        // (one per lane) are loaded a tile ahead.
+        constexpr int kCK = kF8ChunkKeys, kChunks = kTcKeys / kCK, kBoxes = kCK / 16;
+        constexpr int kPerTile = 2 * kChunks, kNc = kF8Converters;
+        const int pw = warp - kSoftmaxWarps;
+        const int total = (kPerTile * n_tiles - pw + kNc - 1) / kNc;   // this warp's chunks
+        const uint32_t stage = sbase + Ly::kOffCS + pw * 2 * Ly::kCodeBytes;
+        const uint8_t* stage_ptr = smem + Ly::kOffCS + pw * 2 * Ly::kCodeBytes;
+        const uint64_t* cbars = code_full[pw];
+        const int32_t* table = block_tables + static_cast<int64_t>(r) * max_blocks;
+        // lane c < 8: raw block id of 16-key piece c of tile t (-1: past the
+        // table; 0 for pieces at or past L, whose codes become zeros)
+        auto piece_ids = [&](int t) -> int {
+            const int key0 = t * kTcKeys + (lane & 7) * 16;
+            if (lane >= 8 || t >= n_tiles || key0 >= L) return 0;
+            return key0 / BS < max_blocks ? __ldg(table + key0 / BS) : -1;
+        };
+        // ids[0] / ids[1]: pieces of tiles id_tile and id_tile + 1
+        int id_tile = 0;
+        int ids[2] = {piece_ids(0), piece_ids(1)};
+        auto request = [&](int n) {   // whole warp: this warp's chunk n
+            const int g = pw + kNc * n, j = g / kPerTile, item = g % kPerTile;
+            const bool k_chunk = item < kChunks;
+            const int e = k_chunk ? item : item - kChunks;
+            const int src_ids = j == id_tile ? ids[0] : ids[1];   // j <= id_tile + 1
+            int bb[kBoxes];
 #pragma unroll
-            for (int c = 0; c < kHalfKeys / 16; ++c) {
-                const int key0 = j * kTcKeys + h * kHalfKeys + c * 16;
-                if (key0 < L) {   // past L the codes are replaced by zeros: reuse the last block
-                    const int lb = key0 / BS;
-                    b = lb < max_blocks ? __ldg(block_tables + static_cast<int64_t>(r) * max_blocks + lb) : -1;
+            for (int x = 0; x < kBoxes; ++x) bb[x] = __shfl_sync(0xffffffffu, src_ids, e * kBoxes + x);
+            if (lane == 0) {
+                const uint32_t bar = smem_u32(&cbars[n & 1]);
+                const uint32_t buf = stage + (n & 1) * Ly::kCodeBytes;
+                mbar_arrive_expect_tx(bar, Ly::kCodeBytes);
+#pragma unroll
+                for (int x = 0; x < kBoxes; ++x) {
+                    const int key0 = j * kTcKeys + e * kCK + x * 16;
+                    int b = bb[x];
                     if (b < 0 || b >= num_blocks) {
                         set_error(err, PA_ERR_OUT_OF_RANGE);
                         b = 0;
                     }
+                    if (k_chunk)   // 16 rows of D codes
+                        tma_load_2d(buf + x * 16 * D, &kmap, 0, (b * n_kv + kvh) * BS + key0 % BS, bar);
+                    else           // D rows of 16 codes (the pool's transposed slab)
+                        tma_load_2d(buf + x * 16 * D, &vmap, key0 % BS, (b * n_kv + kvh) * D, bar);
                 }
-                if (is_k)   // 16 rows of D codes
-                    tma_load_2d(stage + c * 16 * D, map, 0, (b * n_kv + kvh) * BS + key0 % BS, cbar);
-                else        // D rows of 16 codes (the pool's transposed slab)
-                    tma_load_2d(stage + c * 16 * D, map, key0 % BS, (b * n_kv + kvh) * D, cbar);
             }
         };
+        // on a wait that ran out (error recorded): let the copies of chunks n
+        // and n + 1 land (bounded) before the CTA can exit
+        auto drain = [&](int n) {
+            for (int m = n; m < min(n + 2, total); ++m)
+                mbar_wait(smem_u32(&cbars[m & 1]), (m >> 1) & 1, err);
+        };
         if (lane == 0) {
-            prefetch_tensormap(map);
-            if (n_tiles > 0) request(0, 0);   // a tile's first key is always below L
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&vmap);
         }
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % kTcStages;
-            bool ok = true;
-            if (j >= kTcStages) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(smem_u32(&empty_bar[st]), ((j / kTcStages) - 1) & 1, err));
-                if (!ok) mbar_wait(cbar, 0, err);   // half 0 of this tile is in flight
-            }
-            const int keep_tile = L - j * kTcKeys;        // valid keys of this tile (may exceed 128)
-            const uint32_t dst = ring_base + st * Ly::kKBytes;
+        for (int n = 0; n < min(2, total); ++n) request(n);
 #pragma unroll 1
-            for (int h = 0; h < 2 && ok; ++h) {
-                // completion 2j + h of the staging barrier
-                const bool landed = mbar_wait(cbar, h, err);
-                if (!__all_sync(0xffffffffu, landed)) {
-                    // the wait ran out (error recorded): let the copy land (bounded)
-                    // before the CTA can exit
-                    mbar_wait(cbar, h, err);
-                    ok = false;
-                    break;
-                }
-                // 64 x D codes: unit u = 16 codes of one K row (or of one V^T
-                // row's 16-key chunk); each becomes two 16-byte ring chunks
-                for (int u = lane; u < kHalfKeys * D / 16; u += 32) {
-                    uint4 c = *reinterpret_cast<const uint4*>(stage_ptr + u * 16);
-                    uint32_t w[8];
-                    int row, chunk0;   // ring row and first 8-element chunk
-                    if (is_k) {
-                        row = h * kHalfKeys + u / (D / 16);       // key in the tile
-                        chunk0 = 2 * (u % (D / 16));              // d chunk
-                        if (row >= keep_tile) c = make_uint4(0u, 0u, 0u, 0u);
-                    } else {
-                        const int cc = h * (kHalfKeys / 16) + u / D;   // 16-key chunk
-                        row = u % D;                                   // d
-                        chunk0 = 2 * cc;                               // key chunk (8 keys)
-                        c = keep_codes(c, keep_tile - 16 * cc);
-                    }
-                    widen4<T>(c.x, w[0], w[1]);
-                    widen4<T>(c.y, w[2], w[3]);
-                    widen4<T>(c.z, w[4], w[5]);
-                    widen4<T>(c.w, w[6], w[7]);
+        for (int n = 0; n < total; ++n) {
+            const int g = pw + kNc * n, j = g / kPerTile, item = g % kPerTile;
+            const bool k_chunk = item < kChunks;
+            const int e = k_chunk ? item : item - kChunks;
+            const int st = j % kTcStages;
+            if (j >= kTcStages &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&(k_chunk ? k_empty : v_empty)[st]),
+                                                   ((j / kTcStages) - 1) & 1, err))) {
+                drain(n);
+                break;
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&cbars[n & 1]), (n >> 1) & 1, err))) {
+                drain(n);
+                break;
+            }
+            const uint32_t dst = sbase + (k_chunk ? Ly::kOffK : Ly::kOffV) + st * Ly::kKBytes;
+            const int keep_tile = L - j * kTcKeys;        // valid keys of this tile (may exceed 128)
+            // kCK x D codes in units of 16: one K row's d-chunk pair p (or one
+            // V^T row of a 16-key piece), each widened into two 16-byte ring
+            // chunks.  Every 8 lanes touch 8 distinct 16-byte bank groups in
+            // the staging reads and in the ring writes.
+            constexpr int kPer = kCK * D / 512;
+            const uint8_t* src = stage_ptr + (n & 1) * Ly::kCodeBytes;
+            uint4 c[kPer];
+            int row[kPer], chunk0[kPer];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int ch = chunk0 + e;
-                        // K: [keys][d] in 64-column halves; V: [d][keys] in 64-key halves
-                        const uint32_t addr = dst + (ch >> 3) * ((is_k ? kTcKeys : D) * 128) +
-                                              row * 128 + (((ch & 7) ^ (row & 7)) << 4);
-                        st_shared_v4(addr, w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int i = 0; i < kPer; ++i) {
+                int su;   // staging unit
+                if (k_chunk) {
+                    int rl, p;   // row in the chunk, d-chunk pair
+                    if constexpr (D == 128) {
+                        const int gg = lane >> 3, l8 = lane & 7;
+                        rl = 4 * i + 2 * (gg >> 1) + ((l8 >> 2) ^ (gg & 1));
+                        p = l8;
+                    } else {
+                        const int u = lane + 32 * i;
+                        rl = u / (D / 16);
+                        p = u % (D / 16);
                     }
+                    su = rl * (D / 16) + p;
+                    row[i] = e * kCK + rl;
+                    chunk0[i] = 2 * p;
+                } else {
+                    su = lane + 32 * i;                      // piece su / D, row d
+                    row[i] = su % D;
+                    chunk0[i] = 2 * (e * kBoxes + su / D);   // key chunk (8 keys)
                 }
-                fence_proxy_async_smem();   // ring writes -> MMA reads; staging reads -> next TMA
-                __syncwarp();
-                if (lane == 0) {
-                    if (h == 0) request(j, 1);
-                    else if (j + 1 < n_tiles) request(j + 1, 0);
+                c[i] = *reinterpret_cast<const uint4*>(src + su * 16);
+            }
+            if (keep_tile < kTcKeys) {   // the tail tile: keys at or past L become zeros
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    if (k_chunk) {
+                        if (row[i] >= keep_tile) c[i] = make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+                        c[i] = keep_codes(c[i], keep_tile - 8 * chunk0[i]);
+                    }
                 }
             }
-            if (!__all_sync(0xffffffffu, ok)) break;
-            if (lane == 0) mbar_arrive(smem_u32(&full_bar[st]));
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                uint32_t w[8];
+                widen4<T>(c[i].x, w[0], w[1]);
+                widen4<T>(c[i].y, w[2], w[3]);
+                widen4<T>(c[i].z, w[4], w[5]);
+                widen4<T>(c[i].w, w[6], w[7]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int ch = chunk0[i] + h;
+                    const int rw = row[i];
+                    // K: [keys][d] in 64-column halves; V: [d][keys] in 64-key halves
+                    const uint32_t addr = dst + (ch >> 3) * ((k_chunk ? kTcKeys : D) * 128) +
+                                          rw * 128 + (((ch & 7) ^ (rw & 7)) << 4);
+                    st_shared_v4(addr, w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]);
+                }
+            }
+            fence_proxy_async_smem();   // ring writes -> the MMAs' reads
+            __syncwarp();               // and every lane has read the staging buffer
+            if (lane == 0) mbar_arrive(smem_u32(&(k_chunk ? k_full : v_full)[st]));
+            if (n + 2 < total) {
+                const int jn = (pw + kNc * (n + 2)) / kPerTile;
+                if (jn > id_tile + 1) {   // move the id window one tile on
+                    id_tile += 1;
+                    ids[0] = ids[1];
+                    ids[1] = piece_ids(id_tile + 1);
+                }
+                request(n + 2);
+            }
         }
     } else if (warp == kKWarp || warp == kVWarp) {
         // ------------------------------------------------ TMA producers
@@ -666,7 +747,7 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
     const int64_t tiles = (static_cast<int64_t>(a.max_q) * group + kTcTiles * kTcRows - 1) /
                           (kTcTiles * kTcRows);
     dim3 grid(static_cast<unsigned>(tiles), a.cache.n_kv_heads, a.num_reqs);
-    kern<<<grid, kTcThreads, Ly::kDynBytes, s>>>(
+    kern<<<grid, PfWarps<F8>::kThreads, Ly::kDynBytes, s>>>(
         kmap, vmap, a.out, a.out_dtype, static_cast<const T*>(a.q), a.block_tables, a.max_blocks,
         a.q_start, a.context_lens, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
         F8 ? sl2 * a.cache.k_scale : sl2, F8 ? a.cache.v_scale : 1.f, a.err);

@@ -157,3 +157,48 @@ def test_fp8_prefill_needs_scales():
                             torch.tensor([8], dtype=torch.int32, device="cuda"), 8, 0.125, 16)
     assert e.value.status == pa.PA_ERR_INVALID_ARG
     assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("act", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("subnormal", [True, False], ids=["subnormal", "full-range"])
+def test_fp8_prefill_widens_every_code_exactly(act, subnormal):
+    """K = 0 makes attention uniform, so each output row is the plain mean of
+    the visible V values; V holds E4M3 values (scale 1) that the quantizer
+    keeps exactly: only subnormal codes (m * 2^-9), or codes of every
+    exponent.  A widening that flushed or misplaced a code shows up here far
+    above the fp32 rounding of the mean."""
+    n_q, n_kv, d, bs, L = 8, 2, 128, 16, 300
+    rng = np.random.default_rng(31 if subnormal else 32)
+    if subnormal:
+        v = rng.integers(-7, 8, size=(L, n_kv, d)) * 2.0 ** -9
+    else:
+        e = rng.integers(-6, 9, size=(L, n_kv, d)).astype(np.float64)
+        m = rng.integers(0, 8, size=(L, n_kv, d))
+        v = rng.choice([-1.0, 1.0], size=(L, n_kv, d)) * (1 + m / 8) * 2.0 ** e
+        v = np.clip(v, -448.0, 448.0)                           # the largest finite code
+    vt = torch.from_numpy(v).to(act)
+    assert torch.equal(vt.double(), torch.from_numpy(v))       # exact in the activation dtype
+    k = torch.zeros(L, n_kv, d, dtype=act)
+    nb = -(-L // bs) + 2
+    tables = np.arange(-(-L // bs), dtype=np.int32)[None, :]
+    kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    slots = torch.from_numpy(pa.pa_slot_mapping(tables, bs, np.zeros(L, np.int32),
+                                                np.arange(L, dtype=np.int32))).cuda()
+    pa.pa_reshape_and_cache_quant(k.cuda(), vt.cuda(), kc, vc, slots, k_scale=1.0, v_scale=1.0)
+    C = 70
+    q = torch.randn(C, n_q, d, generator=torch.Generator().manual_seed(3)).to(act)
+    out = torch.empty(C, n_q, d, dtype=torch.float32, device="cuda")
+    pa.pa_prefill_chunk(out, q.cuda(), kc, vc, torch.from_numpy(tables).cuda(),
+                        torch.tensor([0, C], dtype=torch.int32, device="cuda"),
+                        torch.tensor([L], dtype=torch.int32, device="cuda"), C, 0.1, bs,
+                        k_scale=1.0, v_scale=1.0)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    got = out.cpu().numpy().astype(np.float64)
+    g = n_q // n_kv
+    for i in range(C):
+        mean = v[:L - C + i + 1].mean(axis=0)                     # [n_kv][d]
+        ref = np.repeat(mean, g, axis=0)
+        bound = 1e-5 * (np.abs(v).max() if not subnormal else 2.0 ** -6)
+        assert np.abs(got[i] - ref).max() <= bound, i
