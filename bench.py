@@ -468,7 +468,7 @@ def run_ours(args, rank, world, local_rank):
             a_.record(stream)
             pa.pa_prefill_chunk(st.p_out, st.p_q_dev, st.k_cache, st.v_cache, st.p_block_tables,
                                 st.query_start_loc, st.p_context_lens, int(st.p_chunk.max()),
-                                wl.scale, wl.block_size, stream=stream)
+                                wl.scale, wl.block_size, stream=stream, **st.kv_scales)
             b_.record(stream)
             if i >= 3:
                 alone.append((a_, b_))

@@ -33,6 +33,8 @@ Workloads (the KV shapes are single transformer layers):
                      clipped), and 4 chunked-prefill requests, each a 512-token
                      chunk on top of U[1024, 8192] cached tokens; the pool is
                      sized to 60e9 bytes of K plus V.
+* ``mixed-llama3-8b-fp8``  the same step (same draws) over an FP8 E4M3 pool with
+                     K and V scale 1/64 (60e9 bytes hold twice the blocks).
 
 Context lengths include the token being decoded: its K/V row is the last row of
 the sequence's logical K/V and is appended by the cache write of the step.
@@ -123,6 +125,14 @@ WORKLOADS = {
                                      shared_prefix_tokens=1024, shared_fraction=0.25,
                                      prefill_requests=4, prefill_chunk=512,
                                      prefill_ctx_range=(1024, 8192)),
+    "mixed-llama3-8b-fp8": Workload("mixed-llama3-8b-fp8", 1005, 192, 32, 8, 128, 32,
+                                    torch.bfloat16, lens_kind="lognormal",
+                                    lens_args=(7.0, 1.0, 16, 32768),
+                                    pool="bytes", pool_arg=60e9,
+                                    shared_prefix_tokens=1024, shared_fraction=0.25,
+                                    prefill_requests=4, prefill_chunk=512,
+                                    prefill_ctx_range=(1024, 8192),
+                                    cache_dtype=torch.float8_e4m3fn, kv_scale=1.0 / 64),
 }
 
 

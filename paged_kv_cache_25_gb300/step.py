@@ -206,7 +206,8 @@ class PagedStep:
                 prefill_events[0].record(side)
             pa.pa_prefill_chunk(t["p_out"], t["p_q_dev"], self.k_cache, self.v_cache,
                                 t["p_block_tables"], t["query_start_loc"], t["p_context_lens"],
-                                int(self.p_chunk.max()), wl.scale, wl.block_size, stream=side)
+                                int(self.p_chunk.max()), wl.scale, wl.block_size, stream=side,
+                                **self.kv_scales)
             if prefill_events is not None:
                 prefill_events[1].record(side)
         decode = pa.pa_decode if wl.q_per_seq == 1 else pa.pa_decode_verify

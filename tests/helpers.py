@@ -50,7 +50,7 @@ def oracle_prefill_rows(step, r: int, rows, threads=None) -> np.ndarray:
     keys 0..L-C+i, i.e. a decode over the truncated logical K/V."""
     dr, wl = step.draws, step.wl
     L, C = int(step.p_lens[r]), int(step.p_chunk[r])
-    k, v = dr.prefill_kv(r, L)
+    k, v = stored_kv(wl, *dr.prefill_kv(r, L))
     q = dr.prefill_q(r)
     outs = []
     for i in rows:

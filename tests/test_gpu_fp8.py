@@ -9,7 +9,7 @@ import oracle
 from paged_kv_cache_25_gb300 import binding as pa
 from paged_kv_cache_25_gb300 import inputs
 from paged_kv_cache_25_gb300.step import PagedStep
-from tests.helpers import half_ulp, max_err, oracle_decode
+from tests.helpers import half_ulp, max_err, oracle_decode, oracle_prefill_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -202,3 +202,25 @@ def test_fp8_prefill_widens_every_code_exactly(act, subnormal):
         ref = np.repeat(mean, g, axis=0)
         bound = 1e-5 * (np.abs(v).max() if not subnormal else 2.0 ** -6)
         assert np.abs(got[i] - ref).max() <= bound, i
+
+
+def test_fp8_mixed_workload_sampled():
+    """The continuous-batching step over an FP8 pool: decode sequences and
+    prefill rows (first, last, middle of each chunk) against the oracle on the
+    dequantized K/V."""
+    wl = inputs.get("mixed-llama3-8b-fp8")
+    st = PagedStep(wl, out_dtype=torch.float32, prefill_out_dtype=torch.float32)
+    st.step()
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    order = np.argsort(st.lens)
+    seqs = sorted({int(order[0]), int(order[-1]), 5, 100}
+                  | {int(i) for i in np.nonzero(st.sharers)[0][:2]})
+    assert max_err(st.out[seqs], oracle_decode(st, seqs)) <= 2e-3
+    qsl = st.query_start_loc.cpu().numpy()
+    for r in range(st.R):
+        C = int(st.p_chunk[r])
+        rows = sorted({0, 1, C // 2, C - 1})
+        got = st.p_out[int(qsl[r]) + np.array(rows)]
+        assert max_err(got, oracle_prefill_rows(st, r, rows)) <= 2e-3
+    assert torch.isfinite(st.out).all() and torch.isfinite(st.p_out).all()
