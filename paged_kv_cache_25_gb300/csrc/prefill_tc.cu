@@ -156,10 +156,15 @@ __device__ __forceinline__ uint4 keep_codes(uint4 c, int keep)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <typename T, int D, int BS, bool F8 = false>
+// T: the MMA operand type (P, K, V and the staged Q); QT: the type q arrives
+// in.  They differ only for FP8 pools with bf16 activations, which run on fp16
+// operands (the codes widen to fp16 in one instruction a pair): each q row is
+// scaled by a power of two 2^-e into fp16 (exact for bf16 values down to 2^-28
+// of the row's largest) and 2^e goes into that row's softmax scale.
+template <typename T, typename QT, int D, int BS, bool F8 = false>
 __global__ void __launch_bounds__(PfWarps<F8>::kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  void* __restrict__ out, pa_dtype out_dtype, const T* __restrict__ q,
+                  void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
                   const int32_t* __restrict__ q_start, const int32_t* __restrict__ context_lens,
                   int n_q, int n_kv, int group, int num_blocks, float scale_log2, float v_scale,
@@ -540,14 +545,56 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const uint4* qp = reinterpret_cast<const uint4*>(
                 q + (static_cast<int64_t>(qs + pos_local) * n_q + head) * D);
             const uint32_t qbase = sbase + Ly::kOffQ + t * Ly::kQBytes;
+            if constexpr (std::is_same<T, QT>::value) {
 #pragma unroll
-            for (int cc = 0; cc < D / 16; ++cc) {
-                const int c = hf * (D / 16) + cc;
-                uint4 v = valid ? __ldg(qp + c) : make_uint4(0, 0, 0, 0);
-                v.x ^= qsign; v.y ^= qsign; v.z ^= qsign; v.w ^= qsign;
-                const uint32_t addr = qbase + (c >> 3) * (kTcRows * 128) + rr * 128 +
-                                      (((c & 7) ^ (rr & 7)) << 4);
-                st_shared_v4(addr, v.x, v.y, v.z, v.w);
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    const int c = hf * (D / 16) + cc;
+                    uint4 v = valid ? __ldg(qp + c) : make_uint4(0, 0, 0, 0);
+                    v.x ^= qsign; v.y ^= qsign; v.z ^= qsign; v.w ^= qsign;
+                    const uint32_t addr = qbase + (c >> 3) * (kTcRows * 128) + rr * 128 +
+                                          (((c & 7) ^ (rr & 7)) << 4);
+                    st_shared_v4(addr, v.x, v.y, v.z, v.w);
+                }
+            } else {
+                // bf16 q -> fp16: the row's largest magnitude (bf16 bits compare
+                // as integers), met with the partner thread's half
+                uint4 v[D / 16];
+                uint32_t amax = 0;
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    v[cc] = valid ? __ldg(qp + hf * (D / 16) + cc) : make_uint4(0, 0, 0, 0);
+                    const uint32_t w4[4] = {v[cc].x, v[cc].y, v[cc].z, v[cc].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        amax = max(amax, max(w4[i] & 0x7FFFu, (w4[i] >> 16) & 0x7FFFu));
+                }
+                // (the slot of key tile 1's maxima: the pair meets at tile 0 before
+                // either writes it again)
+                xmax[1][t][hf][rr] = __uint_as_float(amax << 16);
+                named_bar_sync(bar_id, 64);
+                const float rmax = fmaxf(__uint_as_float(amax << 16), xmax[1][t][hf ^ 1][rr]);
+                int e = 0;
+                if (rmax > 0.f) {
+                    frexpf(rmax, &e);
+                    e = max(e - 15, -100);   // rmax * 2^-e in [2^14, 2^15) unless tiny
+                }
+                scale_log2 = ldexpf(scale_log2, e);
+                const float down = ldexpf(1.f, -e);   // 2^-e, a normal float
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    const int c = hf * (D / 16) + cc;
+                    const uint32_t w4[4] = {v[cc].x, v[cc].y, v[cc].z, v[cc].w};
+                    uint32_t h4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float lo = __uint_as_float(w4[i] << 16) * down;
+                        const float hi = __uint_as_float(w4[i] & 0xFFFF0000u) * down;
+                        h4[i] = Cvt<__half>::pack(lo, hi) ^ qsign;
+                    }
+                    const uint32_t addr = qbase + (c >> 3) * (kTcRows * 128) + rr * 128 +
+                                          (((c & 7) ^ (rr & 7)) << 4);
+                    st_shared_v4(addr, h4[0], h4[1], h4[2], h4[3]);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -717,11 +764,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int D, int BS, bool F8>
+template <typename T, typename QT, int D, int BS, bool F8>
 static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl2)
 {
     using Ly = PfLayout<T, D, F8>;
-    auto kern = prefill_tc_kernel<T, D, BS, F8>;
+    auto kern = prefill_tc_kernel<T, QT, D, BS, F8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -748,31 +795,31 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
                           (kTcTiles * kTcRows);
     dim3 grid(static_cast<unsigned>(tiles), a.cache.n_kv_heads, a.num_reqs);
     kern<<<grid, PfWarps<F8>::kThreads, Ly::kDynBytes, s>>>(
-        kmap, vmap, a.out, a.out_dtype, static_cast<const T*>(a.q), a.block_tables, a.max_blocks,
+        kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
         a.q_start, a.context_lens, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
         F8 ? sl2 * a.cache.k_scale : sl2, F8 ? a.cache.v_scale : 1.f, a.err);
     return cudaGetLastError();
 }
 
-template <typename T, bool F8>
+template <typename T, typename QT, bool F8>
 static cudaError_t run_prefill_tc_dt(const PrefillArgs& a, cudaStream_t s, float sl2)
 {
     const int D = a.cache.head_dim, BS = a.cache.block_size;
-    if (D == 64 && BS == 16) return run_prefill_tc<T, 64, 16, F8>(a, s, sl2);
-    if (D == 64 && BS == 32) return run_prefill_tc<T, 64, 32, F8>(a, s, sl2);
-    if (D == 128 && BS == 16) return run_prefill_tc<T, 128, 16, F8>(a, s, sl2);
-    if (D == 128 && BS == 32) return run_prefill_tc<T, 128, 32, F8>(a, s, sl2);
+    if (D == 64 && BS == 16) return run_prefill_tc<T, QT, 64, 16, F8>(a, s, sl2);
+    if (D == 64 && BS == 32) return run_prefill_tc<T, QT, 64, 32, F8>(a, s, sl2);
+    if (D == 128 && BS == 16) return run_prefill_tc<T, QT, 128, 16, F8>(a, s, sl2);
+    if (D == 128 && BS == 32) return run_prefill_tc<T, QT, 128, 32, F8>(a, s, sl2);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s)
 {
     const float sl2 = a.scale * 1.4426950408889634f;
-    if (a.cache.dtype == PA_BF16) return run_prefill_tc_dt<__nv_bfloat16, false>(a, s, sl2);
-    if (a.cache.dtype == PA_F16) return run_prefill_tc_dt<__half, false>(a, s, sl2);
+    if (a.cache.dtype == PA_BF16) return run_prefill_tc_dt<__nv_bfloat16, __nv_bfloat16, false>(a, s, sl2);
+    if (a.cache.dtype == PA_F16) return run_prefill_tc_dt<__half, __half, false>(a, s, sl2);
     if (a.cache.dtype == PA_FP8_E4M3)   // queries (and the widened K/V) in the activation type
-        return a.cache.act_dtype == PA_BF16 ? run_prefill_tc_dt<__nv_bfloat16, true>(a, s, sl2)
-                                            : run_prefill_tc_dt<__half, true>(a, s, sl2);
+        return a.cache.act_dtype == PA_BF16 ? run_prefill_tc_dt<__half, __nv_bfloat16, true>(a, s, sl2)
+                                            : run_prefill_tc_dt<__half, __half, true>(a, s, sl2);
     return cudaErrorInvalidValue;
 }
 

@@ -83,10 +83,11 @@ def test_fp8_decode_full_size_sampled():
 
 
 def _fp8_prefill_case(seed, specs, n_q, n_kv, d, bs, act, scale, out_dtype=torch.float32,
-                      v_scale=None):
+                      v_scale=None, q_pow2=0):
     """specs: list of (cached tokens, chunk).  The context and the chunk go
     through the quantizing cache write; the oracle attends over the codes
-    times the scale (v_scale for V when given)."""
+    times the scale (v_scale for V when given).  q_pow2 = k multiplies q by
+    2^k and the attention scale by 2^-k (the same scores)."""
     vsc = scale if v_scale is None else v_scale
     rng = np.random.default_rng(seed)
     R = len(specs)
@@ -98,7 +99,8 @@ def _fp8_prefill_case(seed, specs, n_q, n_kv, d, bs, act, scale, out_dtype=torch
     g = torch.Generator().manual_seed(seed)
     ks = [torch.randn(L, n_kv, d, generator=g).to(act) for L in lens]
     vs = [torch.randn(L, n_kv, d, generator=g).to(act) for L in lens]
-    qs = [torch.randn(n, n_q, d, generator=g).to(act) for _, n in specs]
+    qs = [(torch.randn(n, n_q, d, generator=g) * 2.0 ** q_pow2).to(act) for _, n in specs]
+    att = float(np.float32(2.0 ** -q_pow2 / np.sqrt(d)))
     kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
     vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
     seq = np.concatenate([np.full(L, r, np.int32) for r, L in enumerate(lens)])
@@ -112,13 +114,12 @@ def _fp8_prefill_case(seed, specs, n_q, n_kv, d, bs, act, scale, out_dtype=torch
     pa.pa_prefill_chunk(out, torch.cat(qs).cuda(), kc, vc, torch.from_numpy(tables).cuda(),
                         torch.from_numpy(qsl).cuda(),
                         torch.tensor(lens, dtype=torch.int32, device="cuda"),
-                        max(n for _, n in specs), 1.0 / np.sqrt(d), bs,
-                        k_scale=scale, v_scale=vsc)
+                        max(n for _, n in specs), att, bs, k_scale=scale, v_scale=vsc)
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
     kd = [oracle.dequantize_fp8(oracle.quantize_fp8(x, scale), scale) for x in ks]
     vd = [oracle.dequantize_fp8(oracle.quantize_fp8(x, vsc), vsc) for x in vs]
-    ref = np.concatenate(oracle.prefill(qs, kd, vd, float(np.float32(1.0 / np.sqrt(d)))))
+    ref = np.concatenate(oracle.prefill(qs, kd, vd, att))
     return out, ref
 
 
@@ -143,6 +144,16 @@ def test_fp8_prefill_bf16_output_and_unequal_scales():
                                  1.0 / 64, out_dtype=torch.bfloat16, v_scale=0.0125)
     got = out.float().cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got - ref) <= 2e-3 + half_ulp(ref, torch.bfloat16))
+
+
+@pytest.mark.parametrize("q_pow2", [24, -30])
+def test_fp8_prefill_bf16_queries_outside_fp16_range(q_pow2):
+    """bf16 queries far above fp16's largest value or below its smallest normal
+    (the FP8 path multiplies on fp16 operands: each q row is scaled by a power
+    of two first, undone in the row's softmax scale)."""
+    out, ref = _fp8_prefill_case(27, [(200, 70), (0, 33)], 8, 2, 128, 16, torch.bfloat16,
+                                 1.0 / 64, q_pow2=q_pow2)
+    assert max_err(out, ref) <= 2e-3
 
 
 def test_fp8_prefill_needs_scales():
