@@ -27,11 +27,12 @@
 //             and writes P back over its scores in TMEM as hi + lo bf16/fp16
 //             halves (P V keeps ~16 bits of P); the P V MMA takes P straight
 //             from TMEM.  At the end O / l goes to global memory.
-// FP8 (E4M3) pools: the producer warps TMA each key tile's codes into a
-// staging buffer and widen them (exactly) into the same K ring; V is kept in
-// the pool's transposed [d][keys] order and widened into a K-major operand of
-// P V.  Keys at or past the context are written as zeros.  k_scale is folded
-// into the softmax scale and v_scale into the output.
+// FP8 (E4M3) pools: three converter warps replace the two producers; they TMA
+// the codes chunk by chunk into staging buffers and widen them exactly to fp16
+// in the same rings (V kept in the pool's transposed [d][keys] order, a K-major
+// operand of P V); keys at or past the context are written as zeros.  The
+// MMAs run on fp16 operands (bf16 queries are scaled into fp16 per row).
+// k_scale is folded into the softmax scale and v_scale into the output.
 // All waits are bounded; the kernel never traps.
 #include <cuda_fp8.h>
 
@@ -116,31 +117,16 @@ __device__ __forceinline__ void store_row(void* out, int64_t base, int col, cons
     }
 }
 
-// Four E4M3 codes -> four T values (exact), as two packed pairs.  fp16: the
-// hardware pair conversion.  bf16: the code's sign, exponent and mantissa
-// fields moved into place make a bf16 of value code * 2^-120 (E4M3 bias 7,
-// bf16 bias 127; E4M3 subnormals land on bf16 subnormals), which one exact
-// multiply by 2^120 restores.
-template <typename T>
+// Four E4M3 codes -> four fp16 values (exact: every E4M3 value is an fp16
+// normal or zero), as two packed pairs, by the hardware pair conversion.
 __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    if constexpr (std::is_same<T, __half>::value) {
-        asm("{\n\t.reg .b16 a, b;\n\t"
-            "mov.b32 {a, b}, %2;\n\t"
-            "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
-            "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-            : "=r"(lo), "=r"(hi)
-            : "r"(w));
-    } else {
-        const uint32_t x0 = __byte_perm(w, 0u, 0x4140), x1 = __byte_perm(w, 0u, 0x4342);
-        const uint32_t b0 = ((x0 << 4) & 0x07F007F0u) | ((x0 << 8) & 0x80008000u);
-        const uint32_t b1 = ((x1 << 4) & 0x07F007F0u) | ((x1 << 8) & 0x80008000u);
-        // 0x7B80 = 2^120 in bf16; adding -0 keeps the fma a plain exact product
-        asm("fma.rn.bf16x2 %0, %2, %4, %5;\n\t"
-            "fma.rn.bf16x2 %1, %3, %4, %5;"
-            : "=r"(lo), "=r"(hi)
-            : "r"(b0), "r"(b1), "r"(0x7B807B80u), "r"(0x80008000u));
-    }
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Sixteen codes of k-order positions i (low byte first) with the ones at or
@@ -248,6 +234,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
+    static_assert(!F8 || std::is_same<T, __half>::value, "FP8 codes widen to fp16 operands");
     if (F8 && warp >= kSoftmaxWarps && warp < kMmaWarp) {
         // ------------------------------------------------ FP8 converters
         // Chunk g (tile g / (2 kChunks); K chunks first, then V) is widened by
@@ -376,10 +363,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
             for (int i = 0; i < kPer; ++i) {
                 uint32_t w[8];
-                widen4<T>(c[i].x, w[0], w[1]);
-                widen4<T>(c[i].y, w[2], w[3]);
-                widen4<T>(c[i].z, w[4], w[5]);
-                widen4<T>(c[i].w, w[6], w[7]);
+                widen4(c[i].x, w[0], w[1]);
+                widen4(c[i].y, w[2], w[3]);
+                widen4(c[i].z, w[4], w[5]);
+                widen4(c[i].w, w[6], w[7]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int ch = chunk0[i] + h;
@@ -817,7 +804,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s)
     const float sl2 = a.scale * 1.4426950408889634f;
     if (a.cache.dtype == PA_BF16) return run_prefill_tc_dt<__nv_bfloat16, __nv_bfloat16, false>(a, s, sl2);
     if (a.cache.dtype == PA_F16) return run_prefill_tc_dt<__half, __half, false>(a, s, sl2);
-    if (a.cache.dtype == PA_FP8_E4M3)   // queries (and the widened K/V) in the activation type
+    if (a.cache.dtype == PA_FP8_E4M3)   // fp16 operands; q in the activation type
         return a.cache.act_dtype == PA_BF16 ? run_prefill_tc_dt<__half, __nv_bfloat16, true>(a, s, sl2)
                                             : run_prefill_tc_dt<__half, __half, true>(a, s, sl2);
     return cudaErrorInvalidValue;
