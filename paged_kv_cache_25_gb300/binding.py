@@ -28,7 +28,7 @@ __all__ = [
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE = 0, 1, 2, 3
 PA_ERR_WORKSPACE, PA_ERR_TIMEOUT, PA_ERR_CUDA = 4, 5, 6
 _DT = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.float8_e4m3fn: 3}
-PA_FP8_E4M3 = 3
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 
 
 class _Desc(C.Structure):

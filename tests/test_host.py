@@ -152,7 +152,7 @@ def test_cache_write_host_validation():
 
 
 def test_prefill_host_validation():
-    desc = pa._Desc(64, 16, 8, 128, 0)  # fp32 pool: prefill is bf16/fp16 only
+    desc = pa._Desc(64, 16, 8, 128, 0)  # fp32 pool: prefill is bf16/fp16/FP8 only
     f = pa.lib().pa_prefill_chunk
     args = [0x1000, 0, 0x2000, 0x3000, 0x4000, C.byref(desc), 0x5000, 8, 0x6000, 0x7000, 2, 16, 32,
             0.1, 16, None, 0, None]
@@ -164,3 +164,22 @@ def test_prefill_host_validation():
     args[12] = 32
     args[10] = 0
     assert f(*args) == pa.PA_OK                                        # no requests
+
+
+def test_prefill_fp8_host_validation():
+    """FP8 pools need finite positive scales and a bf16/fp16 activation type;
+    head sizes outside {64, 128} are refused before any launch."""
+    f = pa.lib().pa_prefill_chunk
+
+    def call(desc):
+        return f(0x1000, 0, 0x2000, 0x3000, 0x4000, C.byref(desc), 0x5000, 8, 0x6000, 0x7000, 2,
+                 16, 32, 0.1, 16, None, 0, None)
+
+    fp8 = pa.PA_FP8_E4M3
+    assert call(pa._Desc(64, 16, 8, 128, fp8, 0.0, 0.0, pa.PA_BF16)) == pa.PA_ERR_INVALID_ARG
+    assert call(pa._Desc(64, 16, 8, 128, fp8, 0.5, float("nan"), pa.PA_BF16)) == pa.PA_ERR_INVALID_ARG
+    assert call(pa._Desc(64, 16, 8, 128, fp8, 0.5, 0.5, -1)) == pa.PA_ERR_INVALID_ARG
+    assert call(pa._Desc(64, 16, 8, 128, fp8, 0.5, 0.5, pa.PA_F32)) == pa.PA_ERR_INVALID_ARG
+    assert call(pa._Desc(64, 16, 8, 96, fp8, 0.5, 0.5, pa.PA_BF16)) == pa.PA_ERR_UNSUPPORTED
+    assert "FP8" in pa.lib().pa_last_error_message().decode() or \
+        "head_dim" in pa.lib().pa_last_error_message().decode()
