@@ -59,3 +59,24 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True,
                        timeout=300)
     assert p.returncode == 0 and p.stdout.strip() == ""
+
+
+def test_reference_arm_line_on_rank_0():
+    """The reference arm (the oracle on the host cores) prints one JSON line with
+    the bench's keys: value and e2e in the same unit, the cpu_baseline it ran."""
+    import json
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny-fp32", "--steps", "1", "--warmup", "3"], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [x for x in p.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1
+    assert d["warmup"] >= 3 and d["value"] > 0 and d["unit"] == "GB/s"
+    assert d["higher_is_better"] is True and d["config"]["workload"] == "tiny-fp32"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
