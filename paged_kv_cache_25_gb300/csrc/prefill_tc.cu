@@ -64,6 +64,9 @@ struct PfWarps {
     static constexpr int kProducers = F8 ? kF8Converters : 2;
     static constexpr int kMma = kSoftmaxWarps + kProducers;
     static constexpr int kThreads = (kMma + 1) * 32;
+    // the register file is split per SM sub-partition: 20 warps (5 on each)
+    // keep 96 registers a thread, 21 would leave 80 and spill the softmax
+    static_assert(kMma + 1 <= 20, "at most 20 warps");
 };
 constexpr uint32_t kTmemCols = 512;   // S/P_A [0,128) S/P_B [128,256) O_A, O_B from 256
 
