@@ -215,7 +215,7 @@ uint8_t orc_fp8_e4m3_encode(float xf)
 {
     double x = (double)xf;
     if (isnan(x)) return 0x7F;
-    uint8_t sign = x < 0 ? 0x80 : 0x00;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;           /* the sign bit, so -0.0 -> 0x80 */
     double a = fabs(x);
     if (a >= 448.0) return (uint8_t)(sign | 0x7E);        /* saturate */
     /* nearest of the 127 non-negative finite codes, ties to the even code */

@@ -95,9 +95,12 @@ void orc_copy_blocks(const uint8_t* src_k, const uint8_t* src_v, uint8_t* dst_k,
 
 /* [Quant] FP8 E4M3 cache: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
  * bits, subnormals, largest finite 448, no infinities, NaN = all exponent and
- * mantissa bits set.  Encoding rounds to nearest, ties to even, and saturates
- * to +-448.  A cache value is encode(x / scale) with the division in fp32;
- * its meaning is decode(code) * scale. */
+ * mantissa bits set.  Encoding rounds the magnitude to nearest, ties to even,
+ * saturates it to 448, and copies the sign bit of x: -0.0, and a negative
+ * value whose magnitude rounds to zero, give the negative-zero code 0x80, as
+ * IEEE rounding of a signed value does.  NaN gives 0x7F (the pages fix no NaN
+ * code; the tests never write one).  A cache value is encode(x / scale) with
+ * the division in fp32; its meaning is decode(code) * scale. */
 uint8_t orc_fp8_e4m3_encode(float x);
 double  orc_fp8_e4m3_decode(uint8_t code);
 void    orc_quantize_fp8(const float* x, int64_t n, float scale, uint8_t* out);

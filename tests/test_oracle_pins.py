@@ -420,24 +420,46 @@ def test_fp8_e4m3_decode_known_codes():
 def test_fp8_e4m3_round_trip_monotone_ties_saturation():
     vals = [oracle.fp8_decode(c) for c in range(0x7F)]
     assert all(a < b for a, b in zip(vals, vals[1:]))                 # strictly increasing
-    for c in list(range(0x7F)) + list(range(0x81, 0xFF)):
-        assert oracle.fp8_encode(oracle.fp8_decode(c)) == c            # exact round trip
+    # all 254 non-NaN codes, both zeros included: decode then encode is the
+    # identity (decode(0x80) is -0.0, whose sign bit the encoder keeps)
+    codes = list(range(0x7F)) + list(range(0x80, 0xFF))
+    assert len(codes) == 254
+    for c in codes:
+        assert oracle.fp8_encode(oracle.fp8_decode(c)) == c, hex(c)   # exact round trip
+    assert math.copysign(1.0, oracle.fp8_decode(0x80)) == -1.0 and oracle.fp8_decode(0x80) == 0.0
     assert oracle.fp8_encode(1.0625) == 0x38                           # tie -> even mantissa
     assert oracle.fp8_encode(1.1875) == 0x3A
     assert oracle.fp8_encode(1.07) == 0x39                             # nearest
     assert oracle.fp8_encode(1000.0) == 0x7E and oracle.fp8_encode(-1e30) == 0xFE
     assert oracle.fp8_encode(2.0 ** -11) == 0x00                       # below half the smallest
     assert oracle.fp8_encode(3 * 2.0 ** -11) == 0x01                   # rounds up to 2^-9
+    # signed zero: the sign bit is kept, also when a negative magnitude rounds to 0
+    assert oracle.fp8_encode(0.0) == 0x00 and oracle.fp8_encode(-0.0) == 0x80
+    assert oracle.fp8_encode(-2.0 ** -11) == 0x80 and oracle.fp8_encode(-1e-30) == 0x80
+    assert oracle.fp8_encode(-3 * 2.0 ** -11) == 0x81
+    # ties at the top: 464 lies halfway between 448 (even mantissa) and 480 (not
+    # finite in E4M3), so it saturates like anything larger
+    assert oracle.fp8_encode(464.0) == 0x7E and oracle.fp8_encode(-470.0) == 0xFE
 
 
 def test_fp8_e4m3_matches_library_cast_in_range():
-    """torch's float8_e4m3fn cast is round-to-nearest-even; compare in range."""
+    """torch's float8_e4m3fn cast is round-to-nearest-even and keeps the sign
+    of zero; it turns magnitudes of 480 and more into NaN instead of
+    saturating, so saturation is compared as a clamp to +-448 before the cast."""
     g = torch.Generator().manual_seed(1)
-    x = torch.cat([torch.randn(4000, generator=g) * 60, torch.randn(2000, generator=g) * 0.01])
-    x = x.clamp(-440, 440)
+    x = torch.cat([torch.randn(4000, generator=g) * 60, torch.randn(2000, generator=g) * 0.01,
+                   torch.randn(2000, generator=g) * 1e-3,          # many round to +-0
+                   torch.tensor([0.0, -0.0, -1e-9, 1e-9, 447.9, 448.0, 449.0, 463.9, 464.0,
+                                 464.1, 479.0, 480.0, 1000.0, 3.0e38, -448.5, -500.0, -3.0e38])])
     ours = oracle.quantize_fp8(x, 1.0)
-    lib = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    lib = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(ours, lib)
+    assert (ours == 0x80).sum() > 0 and (ours == 0x00).sum() > 0 and (ours == 0xFE).sum() > 0
+    # every code's value, positive and negative zero included, casts to itself
+    all_vals = torch.tensor([oracle.fp8_decode(c) for c in range(0x7F)] +
+                            [oracle.fp8_decode(c) for c in range(0x80, 0xFF)], dtype=torch.float32)
+    assert np.array_equal(oracle.quantize_fp8(all_vals, 1.0),
+                          all_vals.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
 
 
 def test_fp8_quantize_divides_in_fp32_then_rounds():
