@@ -85,7 +85,9 @@ typedef struct {
 /* ---------------------------------------------------------------- cache write
  * Append K/V rows into their slots ("Life of a prompt": one new K and V
  * vector per token go into the next free slot of the sequence's blocks).
- *   k, v          : [num_tokens][n_kv_heads][head_dim], contiguous, cache dtype.
+ *   k, v          : [num_tokens][n_kv_heads][head_dim], contiguous, cache dtype
+ *                   (for FP8 pools: E4M3 codes, copied as they are; the V codes
+ *                   land in the pool's transposed V layout described above).
  *   k_cache/v_cache: pools as in the layout above; written in place.
  *   slot_mapping  : int64 [num_tokens] on the device.  slot < 0 means "skip this
  *                   token" (padding).  slot >= num_blocks*block_size sets
@@ -216,7 +218,10 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
  *                     query_start_loc[0] = 0; C_r = difference of neighbours.
  *   context_lens    : int32 [num_reqs] on the device: total tokens L_r of
  *                     request r including the chunk (C_r <= L_r).
- *   max_query_len   : host value >= every C_r (sizes the grid).
+ *   max_query_len   : host value >= every C_r (sizes the grid).  A request
+ *                     with C_r > max_query_len sets PA_ERR_OUT_OF_RANGE in the
+ *                     device error word (its rows past max_query_len are not
+ *                     written).
  *   workspace       : reserved; pass NULL / 0 (pa_prefill_workspace_size is 0).
  * bf16, fp16 and FP8 E4M3 pools (f32 pools return PA_ERR_UNSUPPORTED).  FP8
  * pools keep V transposed per block as for decode; their codes are widened

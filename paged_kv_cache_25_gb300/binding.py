@@ -154,10 +154,12 @@ def pa_status_string(st: int) -> str:
     return lib().pa_status_string(st).decode()
 
 
-def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None):
-    """k, v [T][n_kv][d] -> pools [NB][n_kv][bs][d] at slot_mapping (int64 [T])."""
+def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None, k_scale=None,
+                         v_scale=None):
+    """k, v [T][n_kv][d] -> pools [NB][n_kv][bs][d] at slot_mapping (int64 [T]).
+    FP8 pools take rows of E4M3 codes (copied as they are) and their scales."""
     assert k.is_contiguous() and v.is_contiguous() and slot_mapping.dtype == torch.int64
-    d = _desc(k_cache)
+    d = _desc(k_cache, k_scale, v_scale)
     _check(lib().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                       _ptr(slot_mapping), int(k.shape[0]), C.byref(d),
                                       _stream(stream)), "pa_reshape_and_cache")

@@ -274,7 +274,7 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
                                const int64_t* slot_mapping, int num_tokens,
                                const pa_cache_desc* cache, void* stream)
 {
-    pa_status st = check_cache(cache);
+    pa_status st = check_cache(cache, false);
     if (st != PA_OK) return st;
     if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
     if (num_tokens == 0) return ok();
@@ -286,8 +286,14 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
         return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
     unsigned* err = device_error_word();
     if (!err) return fail(PA_ERR_CUDA, "cannot locate the device error word");
-    cudaError_t e = launch_cache_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, *cache, err,
-                                       static_cast<cudaStream_t>(stream));
+    // FP8 pools keep V transposed per block: the rows (codes already) go
+    // through the FP8 writer, which copies them and lays V out that way
+    cudaError_t e = cache->dtype == PA_FP8_E4M3
+                        ? launch_cache_write_fp8(k, v, PA_FP8_E4M3, k_cache, v_cache, slot_mapping,
+                                                 num_tokens, *cache, err,
+                                                 static_cast<cudaStream_t>(stream))
+                        : launch_cache_write(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                             *cache, err, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cache write launch");
     return ok();
 }

@@ -54,10 +54,11 @@ cudaError_t launch_cache_write(const void* k, const void* v, void* kc, void* vc,
     return cudaGetLastError();
 }
 
-// Quantizing write into an FP8 E4M3 pool: one thread turns 16 input elements
-// of one (token, head) row into 16 codes: code = e4m3_rn_satfinite(x / scale)
-// with x / scale an IEEE fp32 division.  K codes are one 16-byte store; V
-// codes go to the transposed V slab, one column of [head_dim][block_size].
+// Write into an FP8 E4M3 pool: one thread turns 16 input elements of one
+// (token, head) row into 16 codes: code = e4m3_rn_satfinite(x / scale) with
+// x / scale an IEEE fp32 division (or, for rows given as codes, the codes
+// themselves).  K codes are one 16-byte store; V codes go to the transposed V
+// slab, one column of [head_dim][block_size].
 template <typename TI>
 __device__ __forceinline__ float load_as_float(const TI* p, int i);
 template <> __device__ __forceinline__ float load_as_float<float>(const float* p, int i) { return p[i]; }
@@ -87,6 +88,19 @@ __device__ __forceinline__ uint4 quant16(const TI* src, float scale)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Sixteen elements of a row as E4M3 codes: quantized from fp32/fp16/bf16, or,
+// for rows that already hold codes (TI = uint8_t), the 16 bytes themselves.
+template <typename TI>
+__device__ __forceinline__ uint4 codes16(const TI* src, float scale)
+{
+    return quant16(src, scale);
+}
+template <>
+__device__ __forceinline__ uint4 codes16<uint8_t>(const uint8_t* src, float)
+{
+    return __ldcs(reinterpret_cast<const uint4*>(src));
+}
+
 template <typename TI>
 __global__ void __launch_bounds__(256)
 cache_write_fp8_kernel(const TI* __restrict__ k, const TI* __restrict__ v, uint4* __restrict__ kc,
@@ -109,9 +123,9 @@ cache_write_fp8_kernel(const TI* __restrict__ k, const TI* __restrict__ v, uint4
     const int64_t b = slot / block_size, o = slot - b * block_size;
     const int64_t dst = ((b * n_kv + h) * block_size + o) * pieces_per_row + c;
     const int64_t src = i * 16;                   // element offset of this piece
-    kc[dst] = quant16(k + src, k_scale);
+    kc[dst] = codes16(k + src, k_scale);
     // V codes are stored transposed per (block, head): [head_dim][block_size]
-    const uint4 vq = quant16(v + src, v_scale);
+    const uint4 vq = codes16(v + src, v_scale);
     uint8_t* vcol = reinterpret_cast<uint8_t*>(vc) +
                     ((b * n_kv + h) * (pieces_per_row * 16) + c * 16) * block_size + o;
     const uint32_t w[4] = {vq.x, vq.y, vq.z, vq.w};
@@ -136,6 +150,7 @@ cudaError_t launch_cache_write_fp8(const void* k, const void* v, pa_dtype in_dty
         c.v_scale, err)
     if (in_dtype == PA_BF16) PA_QW(__nv_bfloat16);
     else if (in_dtype == PA_F16) PA_QW(__half);
+    else if (in_dtype == PA_FP8_E4M3) PA_QW(uint8_t);   // codes already: copied, V transposed
     else PA_QW(float);
 #undef PA_QW
     return cudaGetLastError();

@@ -156,8 +156,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                   void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
                   const int32_t* __restrict__ q_start, const int32_t* __restrict__ context_lens,
-                  int n_q, int n_kv, int group, int num_blocks, float scale_log2, float v_scale,
-                  unsigned* err)
+                  int max_q, int n_q, int n_kv, int group, int num_blocks, float scale_log2,
+                  float v_scale, unsigned* err)
 {
     using Ly = PfLayout<T, D, F8>;
     constexpr int kMmaWarp = PfWarps<F8>::kMma;
@@ -175,6 +175,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int L = __ldg(context_lens + r);
     const int rows_total = C * group;
     const int row0 = blk * (kTcTiles * kTcRows);
+    // the grid covers max_q rows per request: a longer chunk would leave its
+    // last rows unwritten, so it is flagged (once, by the request's first CTA)
+    if (C > max_q && blk == 0 && threadIdx.x == 0) set_error(err, PA_ERR_OUT_OF_RANGE);
     if (row0 >= rows_total) return;
     if (C > L || C < 0) {
         if (threadIdx.x == 0) set_error(err, PA_ERR_OUT_OF_RANGE);
@@ -786,7 +789,7 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
     dim3 grid(static_cast<unsigned>(tiles), a.cache.n_kv_heads, a.num_reqs);
     kern<<<grid, PfWarps<F8>::kThreads, Ly::kDynBytes, s>>>(
         kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
-        a.q_start, a.context_lens, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
+        a.q_start, a.context_lens, a.max_q, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
         F8 ? sl2 * a.cache.k_scale : sl2, F8 ? a.cache.v_scale : 1.f, a.err);
     return cudaGetLastError();
 }

@@ -45,6 +45,49 @@ def oracle_decode(step, seqs=None, threads=None) -> np.ndarray:
     return oracle.decode(q, ks, vs, wl.scale, threads=threads)
 
 
+def oracle_decode_all(step, chunk: int = 32, threads=None) -> np.ndarray:
+    """fp64 outputs of every decode sequence of a PagedStep, computed chunk
+    sequences at a time (bounded host memory at full workload sizes):
+    [B][n_q][d], or [B][q_per_seq][n_q][d] for several query rows per
+    sequence (query i at position L - q_per_seq + i, causal among the rows)."""
+    dr, wl = step.draws, step.wl
+    prefix = dr.prefix_kv() if step.prefix else None
+    q = dr.q()
+    outs = []
+    for s0 in range(0, wl.batch, chunk):
+        seqs = range(s0, min(wl.batch, s0 + chunk))
+        ks, vs = [], []
+        for s in seqs:
+            k, v = dr.seq_kv(s, int(step.lens[s]), bool(step.sharers[s]), prefix)
+            k, v = stored_kv(wl, k, v)
+            ks.append(k); vs.append(v)
+        if wl.q_per_seq == 1:
+            outs.append(oracle.decode(q[s0:s0 + len(ks)], ks, vs, wl.scale, threads=threads))
+        else:
+            outs.append(np.stack(oracle.prefill([q[s] for s in seqs], ks, vs, wl.scale,
+                                                threads=threads)))
+    return np.concatenate(outs)
+
+
+def oracle_prefill_all(step, threads=None) -> np.ndarray:
+    """fp64 outputs of every chunked-prefill row of a PagedStep, [sum C][n_q][d]."""
+    dr, wl = step.draws, step.wl
+    qs, ks, vs = [], [], []
+    for r in range(step.R):
+        k, v = stored_kv(wl, *dr.prefill_kv(r, int(step.p_lens[r])))
+        qs.append(dr.prefill_q(r)); ks.append(k); vs.append(v)
+    return np.concatenate(oracle.prefill(qs, ks, vs, wl.scale, threads=threads))
+
+
+def check_low_precision(got: torch.Tensor, ref: np.ndarray, dtype: torch.dtype,
+                        tol: float = 2e-3) -> float:
+    """Output stored in bf16/fp16: |got - ref| <= tol + half an ulp of ref in
+    that dtype (the store's own rounding).  Returns the largest excess."""
+    g = got.detach().float().cpu().numpy().astype(np.float64)
+    excess = np.abs(g - ref) - (tol + half_ulp(ref, dtype))
+    return float(excess.max())
+
+
 def oracle_prefill_rows(step, r: int, rows, threads=None) -> np.ndarray:
     """fp64 outputs of chosen query rows of prefill request r: row i attends
     keys 0..L-C+i, i.e. a decode over the truncated logical K/V."""

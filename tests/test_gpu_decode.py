@@ -9,7 +9,7 @@ import oracle
 from paged_kv_cache_25_gb300 import binding as pa
 from paged_kv_cache_25_gb300 import inputs
 from paged_kv_cache_25_gb300.step import PagedStep
-from tests.helpers import TOL, half_ulp, max_err, oracle_decode
+from tests.helpers import TOL, check_low_precision, half_ulp, max_err, oracle_decode, oracle_decode_all
 
 pytestmark = pytest.mark.gpu
 
@@ -251,26 +251,21 @@ def test_decode_host_checks_launch_nothing():
 
 # ------------------------------------------------------------------ full-size workloads
 
-def _sample(lens, k=6, seed=0):
-    order = np.argsort(lens)
-    picks = {int(order[0]), int(order[-1])}
-    rng = np.random.default_rng(seed)
-    picks.update(int(x) for x in rng.choice(len(lens), size=min(k, len(lens)), replace=False))
-    return sorted(picks)
-
-
 @pytest.mark.parametrize("name", ["llama3-8b-bf16", "opt13b-fp16", "mixed-llama3-8b-bf16"])
-def test_decode_full_size_sampled(name):
+def test_decode_full_size_all_outputs(name):
+    """Every output of the full-size decode batch (all sequences x all query
+    heads x all head-dim elements), once stored in fp32 (<= 2e-3) and once in
+    the workload's own dtype, as the bench times it (<= 2e-3 + half an ulp)."""
     wl = inputs.get(name)
     st = PagedStep(wl, out_dtype=torch.float32)
     st.step()
+    out_lp = torch.full(tuple(st.out.shape), float("nan"), dtype=wl.dtype, device="cuda")
+    pa.pa_decode(out_lp, st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens,
+                 wl.scale, wl.block_size, st.workspace)
     torch.cuda.synchronize()
     _check_clean()
-    seqs = _sample(st.lens)
-    if st.sharers.any():
-        seqs += [int(i) for i in np.nonzero(st.sharers)[0][:3]]
-    ref = oracle_decode(st, seqs)
-    err = max_err(st.out[seqs], ref)
+    ref = oracle_decode_all(st)
+    assert ref.shape == tuple(st.out.shape)
+    err = max_err(st.out, ref)
     assert err <= TOL[wl.dtype], err
-    # every output finite (NaN sentinels never leak)
-    assert torch.isfinite(st.out).all()
+    assert check_low_precision(out_lp, ref, wl.dtype) <= 0.0

@@ -7,7 +7,7 @@ import oracle
 from paged_kv_cache_25_gb300 import binding as pa
 from paged_kv_cache_25_gb300 import inputs
 from paged_kv_cache_25_gb300.step import PagedStep
-from tests.helpers import TOL, half_ulp, max_err, oracle_prefill_rows
+from tests.helpers import TOL, check_low_precision, half_ulp, max_err, oracle_prefill_all
 
 pytestmark = pytest.mark.gpu
 
@@ -85,20 +85,40 @@ def test_prefill_chunk_of_one_matches_decode():
     assert max_err(out, ref) <= 2e-3
 
 
-def test_prefill_mixed_workload_sampled_rows():
+def test_prefill_mixed_workload_all_rows():
+    """The mixed step's four 512-row chunks over 1024-8192 cached tokens: every
+    output row of every head, stored in fp32 (<= 2e-3) and in bf16 (<= 2e-3 +
+    half an ulp), against the oracle's chunked prefill."""
     wl = inputs.get("mixed-llama3-8b-bf16")
     st = PagedStep(wl, out_dtype=torch.float32, prefill_out_dtype=torch.float32)
     st.step()
+    out_lp = torch.full(tuple(st.p_out.shape), float("nan"), dtype=wl.dtype, device="cuda")
+    pa.pa_prefill_chunk(out_lp, st.p_q_dev, st.k_cache, st.v_cache, st.p_block_tables,
+                        st.query_start_loc, st.p_context_lens, int(st.p_chunk.max()), wl.scale,
+                        wl.block_size)
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
-    qsl = st.query_start_loc.cpu().numpy()
-    for r in range(st.R):
-        C = int(st.p_chunk[r])
-        rows = sorted({0, 1, 2, C // 2, C - 2, C - 1})
-        ref = oracle_prefill_rows(st, r, rows)
-        got = st.p_out[int(qsl[r]) + np.array(rows)]
-        assert max_err(got, ref) <= 2e-3
-    assert torch.isfinite(st.p_out).all()
+    ref = oracle_prefill_all(st)
+    assert ref.shape == tuple(st.p_out.shape)
+    assert max_err(st.p_out, ref) <= 2e-3
+    assert check_low_precision(out_lp, ref, wl.dtype) <= 0.0
+
+
+def test_prefill_chunk_longer_than_max_query_len_is_flagged():
+    """max_query_len sizes the grid; a request whose chunk is longer is reported
+    in the device error word instead of silently leaving rows unwritten."""
+    d, bs, n_q, n_kv, C = 64, 16, 8, 2, 300
+    nb = 5                                          # table entries reuse blocks 0..4
+    tables = np.arange(-(-C // bs), dtype=np.int32)[None, :] % nb
+    kc = torch.zeros((nb, n_kv, bs, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    q = torch.zeros((C, n_q, d), dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros((C, n_q, d), dtype=torch.float32, device="cuda")
+    pa.pa_prefill_chunk(o, q, kc, vc, torch.from_numpy(np.ascontiguousarray(tables)).cuda(),
+                        torch.tensor([0, C], dtype=torch.int32, device="cuda"),
+                        torch.tensor([C], dtype=torch.int32, device="cuda"), 64, 0.125, bs)
+    assert pa.pa_get_device_error() == pa.PA_ERR_OUT_OF_RANGE
+    assert pa.pa_get_device_error() == 0
 
 
 def test_prefill_negative_and_zero_scale():

@@ -8,7 +8,7 @@ import torch
 import oracle
 from paged_kv_cache_25_gb300 import binding as pa
 from paged_kv_cache_25_gb300 import inputs
-from tests.helpers import TOL, max_err, stored_kv
+from tests.helpers import TOL, check_low_precision, max_err, oracle_decode_all, stored_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -177,20 +177,20 @@ def test_verify_host_checks():
     assert pa.pa_get_device_error() == 0
 
 
-def test_verify_full_size_workload_sampled():
+def test_verify_full_size_workload_all_outputs():
     """The Llama-3-8B batch with 4 query rows per sequence, as the bench runs
-    it (cache write of the 4 new rows, then the multi-query decode)."""
+    it (cache write of the 4 new rows, then the multi-query decode): every
+    output, in fp32 and in bf16."""
     from paged_kv_cache_25_gb300.step import PagedStep
     wl = inputs.get("llama3-8b-bf16-verify4")
     st = PagedStep(wl, out_dtype=torch.float32)
     st.step()
+    out_lp = torch.full(tuple(st.out.shape), float("nan"), dtype=wl.dtype, device="cuda")
+    pa.pa_decode_verify(out_lp, st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens,
+                        wl.scale, wl.block_size, st.workspace)
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
-    order = np.argsort(st.lens)
-    seqs = sorted({int(order[0]), int(order[-1]), 3, 77, 150, 201})
-    dr = st.draws
-    q = dr.q()
-    ks, vs = zip(*(dr.seq_kv(s, int(st.lens[s])) for s in seqs))
-    ref = np.stack(oracle.prefill([q[s] for s in seqs], list(ks), list(vs), wl.scale))
-    assert max_err(st.out[seqs], ref) <= TOL[wl.dtype]
-    assert torch.isfinite(st.out).all()
+    ref = oracle_decode_all(st)
+    assert ref.shape == tuple(st.out.shape)
+    assert max_err(st.out, ref) <= TOL[wl.dtype]
+    assert check_low_precision(out_lp, ref, wl.dtype) <= 0.0

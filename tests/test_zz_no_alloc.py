@@ -5,8 +5,9 @@ offers plugins no allocator, or a latency-critical loop that cannot pay for
 cudaMalloc's synchronisation) pass only inputs and outputs; the split-K scratch
 is a fixed array inside the library.  This file is collected last on purpose.
 Its checks: through the C ABI, two calls in a row each match pa_decode with a
-caller workspace within the decode tolerance, and a batch too large for the
-fixed scratch is refused before anything runs.
+caller workspace, and the CPU oracle's fp64 attention, within the decode
+tolerance; a batch too large for the fixed scratch is refused before anything
+runs.
 """
 import pytest
 import torch
@@ -14,7 +15,7 @@ import torch
 from paged_kv_cache_25_gb300 import binding as pa
 from paged_kv_cache_25_gb300 import inputs
 from paged_kv_cache_25_gb300.step import PagedStep
-from tests.helpers import TOL
+from tests.helpers import TOL, max_err, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +36,7 @@ def test_no_alloc_matches_workspace_decode_twice():
                                        wl.block_size, st.max_blocks * wl.block_size)
     assert 0 < need <= pa.PA_DECODE_NO_ALLOC_SCRATCH_BYTES
     ref = st.out.clone()
+    exact = oracle_decode(st)                # fp64 attention of the same inputs
     for _ in range(2):
         out = torch.full_like(ref, float("nan"))
         pa.pa_decode_no_alloc(out, st.q, st.k_cache, st.v_cache, st.block_tables,
@@ -42,6 +44,7 @@ def test_no_alloc_matches_workspace_decode_twice():
         torch.cuda.synchronize()
         assert pa.pa_get_device_error() == 0
         assert float((out - ref).abs().max()) <= TOL[wl.dtype]
+        assert max_err(out, exact) <= TOL[wl.dtype]
 
 
 def test_no_alloc_rejects_batches_beyond_its_scratch():
