@@ -40,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
 # sources are byte-identical to what was profiled (sha256 of DECODE_SOURCES).
 NCU_TRAFFIC = {
-    # one-pass ncu captures (--metrics dram__bytes_read.sum,dram__bytes_write.sum,
-    # full-size workload, 4th launch); profiles/decode_dram_full_size.md
+    # one-pass ncu captures (--metrics dram__bytes_read.sum,dram__bytes_write.sum
+    # of the decode kernel, 4th launch)
     ("llama3-8b-bf16", 256, "ad80b383e235384f"): 2371977216 + 13616640,
     ("llama3-8b-fp8", 256, "ad80b383e235384f"): 1188184576 + 12948224,
     ("llama3-8b-bf16-verify4", 256, "ad80b383e235384f"): 2384849152 + 44538624,
@@ -238,6 +238,186 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- our arm
+def _ev():
+    import torch
+    return torch.cuda.Event(enable_timing=True)
+
+
+def _nvtx(name):
+    import torch
+    return torch.cuda.nvtx.range(name)
+
+
+def _flush_buffer(st, dev):
+    """A 2 x L2 buffer to write before each timed step when the pool would
+    otherwise sit in L2 (None when the pool is larger than that)."""
+    import torch
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool_bytes = (st.k_cache.numel() * st.k_cache.element_size() +
+                  st.v_cache.numel() * st.v_cache.element_size())
+    if pool_bytes >= 2 * l2_bytes:
+        return None, l2_bytes, pool_bytes
+    return torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev), l2_bytes, pool_bytes
+
+
+def _l2_note(flush, l2_bytes, pool_bytes, kv_unique):
+    if flush is None:
+        return (f"inputs larger than L2 ({pool_bytes / 1e9:.2f} GB pool, "
+                f"{kv_unique / 1e9:.2f} GB of K/V read per step); no flush")
+    return (f"L2 flushed before every timed step (a {2 * l2_bytes >> 20} MiB write, outside "
+            f"the step's events); the pool ({pool_bytes / 1e6:.0f} MB) would fit in L2")
+
+
+def profiled_steps(st, stream, n, flush=None):
+    """n steps, each bracketed by CUDA events on the step's stream, the decode
+    kernel by the library's profiling events and the chunked prefill (if any)
+    by events on its side stream.  Returns per-step lists in ms: step, decode
+    kernel, prefill kernel (inside the step)."""
+    import torch
+    from paged_kv_cache_25_gb300 import binding as pa
+    ev = [(_ev(), _ev()) for _ in range(n)]
+    dk = [(_ev(), _ev()) for _ in range(n)]
+    pf = [(_ev(), _ev()) for _ in range(n)] if st.R else [None] * n
+    for i in range(n):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        pa.pa_set_profile_events(*dk[i])
+        st.step(prefill_events=pf[i])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    pa.pa_set_profile_events(None, None)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = [a.elapsed_time(b) for a, b in dk]
+    pf_ms = [a.elapsed_time(b) for a, b in pf] if st.R else None
+    return step_ms, dec_ms, pf_ms
+
+
+def prefill_alone_ms(st, stream, n):
+    """The step's chunked-prefill call timed on its own (inside the step it
+    shares the SMs with the decode launched beside it)."""
+    import torch
+    from paged_kv_cache_25_gb300 import binding as pa
+    wl = st.wl
+    pairs = []
+    for i in range(n + 3):
+        a_, b_ = _ev(), _ev()
+        a_.record(stream)
+        pa.pa_prefill_chunk(st.p_out, st.p_q_dev, st.k_cache, st.v_cache, st.p_block_tables,
+                            st.query_start_loc, st.p_context_lens, int(st.p_chunk.max()),
+                            wl.scale, wl.block_size, stream=stream, **st.kv_scales)
+        b_.record(stream)
+        if i >= 3:
+            pairs.append((a_, b_))
+    torch.cuda.synchronize()
+    return [a_.elapsed_time(b_) for a_, b_ in pairs]
+
+
+def _dtype_name(wl):
+    if wl.cache_dtype is not None:
+        return "e4m3 K/V, f16 products"
+    return {"torch.bfloat16": "bf16", "torch.float16": "f16", "torch.float32": "f32"}[str(wl.dtype)]
+
+
+def _traffic(name, batch):
+    src = _src_hash(DECODE_SOURCES)
+    return NCU_TRAFFIC.get((name, batch, src))
+
+
+def _prefill_roofline(st, pf_ms):
+    flops = st.prefill_flops()
+    tf, tf_src = _peaks_tensor()
+    achieved = flops / (statistics.mean(pf_ms) * 1e-3) / 1e12
+    return flops, {
+        "bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s",
+        "frac": achieved / tf, "traffic": None, "kernel": "prefill_tc_kernel",
+        "peak_source": tf_src, "kernel_ms_mean": statistics.mean(pf_ms),
+        "kernel_ms_median": statistics.median(pf_ms), "launches_timed": len(pf_ms),
+        "timing": "kernel alone (in the step it overlaps the decode)"}
+
+
+def measure_workload(name, dev, phys, target_s=0.6, min_steps=50, max_steps=3000):
+    """One record per workload: a fresh PagedStep, 10 warm-up steps, then
+    at least min_steps steps (as many as fit in ~target_s) with per-step
+    events; medians, the decode kernel's roofline, clocks over the loop."""
+    import torch
+    from paged_kv_cache_25_gb300 import binding as pa
+    from paged_kv_cache_25_gb300 import inputs
+    from paged_kv_cache_25_gb300.step import PagedStep
+    wl = inputs.get(name)
+    t0 = time.perf_counter()
+    st = PagedStep(wl, device=dev)
+    setup_s = time.perf_counter() - t0
+    stream = torch.cuda.current_stream(dev)
+    flush, l2_bytes, pool_bytes = _flush_buffer(st, dev)
+    for _ in range(10):
+        st.step()
+    torch.cuda.synchronize(dev)
+    probe, _, _ = profiled_steps(st, stream, 5, flush)
+    n = int(min(max_steps, max(min_steps, target_s / max(statistics.median(probe), 1e-3) * 1e3)))
+    clocks = ClockSampler(phys)
+    clocks.start()
+    time.sleep(0.3)
+    with _nvtx(f"workload {name}"):
+        step_ms, dec_ms, pf_ms = profiled_steps(st, stream, n, flush)
+    clk = clocks.stop()
+    assert pa.pa_get_device_error() == 0
+    kv_unique = st.kv_bytes_unique()
+    peak, peak_kind = _peaks()
+    med = statistics.median(step_ms)
+    dmean, dmed = statistics.mean(dec_ms), statistics.median(dec_ms)
+    achieved = kv_unique / (dmean * 1e-3) / 1e9
+    rec = {
+        "workload": wl.name, "dtype": _dtype_name(wl), "batch": wl.batch,
+        "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
+        "block_size": wl.block_size, "q_per_seq": wl.q_per_seq, "prefill_requests": st.R,
+        "num_blocks": st.num_blocks, "steps": n, "warmup": 10,
+        "ms_per_step_median": med, "ms_per_step_mean": statistics.mean(step_ms),
+        "value": kv_unique / (med * 1e-3) / 1e9, "unit": "GB/s",
+        "decode_tokens_per_s": wl.batch * wl.q_per_seq / (med * 1e-3),
+        "steps_per_s": 1e3 / med,
+        "kv_bytes_unique_per_step": kv_unique,
+        "kv_bytes_block_granular_per_step": st.kv_bytes_block_granular(),
+        "kv_bytes_logical_per_step": st.kv_bytes_logical(),
+        "decode_kernel_ms_mean": dmean, "decode_kernel_ms_median": dmed,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _traffic(wl.name, wl.batch),
+                     "kernel": "decode_mma_kernel", "peak_source": f"hbm_gbs ({peak_kind})"},
+        "l2": _l2_note(flush, l2_bytes, pool_bytes, kv_unique),
+        "clocks": clk, "setup_s": setup_s,
+    }
+    if st.R:
+        rec["prefill_kernel_ms_in_step_median"] = statistics.median(pf_ms)
+        rec["prefill_tokens_per_s"] = int(st.p_chunk.sum()) / (med * 1e-3)
+        alone = prefill_alone_ms(st, stream, max(50, min(n, 200)))
+        rec["prefill_flops_per_step"], rec["roofline_prefill"] = _prefill_roofline(st, alone)
+    if wl.batch <= 64 and wl.cache_dtype is None and wl.q_per_seq == 1:
+        # BASELINE's CPU plan: the oracle single-threaded on the small configs
+        rec["cpu_baseline_1thread"] = oracle_one_thread(st)
+    del st
+    torch.cuda.empty_cache()
+    return rec
+
+
+def oracle_one_thread(st):
+    """The oracle over the whole decode batch of a small workload on one host
+    thread (inputs regenerated from the seeded draws, packing excluded)."""
+    import oracle
+    dr, wl = st.draws, st.wl
+    kv = [dr.seq_kv(s, int(st.lens[s])) for s in range(wl.batch)]
+    q = dr.q()
+    t0 = time.perf_counter()
+    oracle.decode(q, [k for k, _ in kv], [v for _, v in kv], wl.scale, threads=1)
+    t = time.perf_counter() - t0
+    kvb = st.kv_bytes_logical()
+    return {"value": kvb / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": t, "sample": f"all {wl.batch} decode sequences, one thread"}
+
+
+OTHER_WORKLOADS = ("tiny-fp32", "tinyllama-bf16", "opt13b-fp16", "mixed-llama3-8b-bf16",
+                   "llama3-8b-fp8", "llama3-8b-bf16-verify4", "mixed-llama3-8b-fp8")
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from paged_kv_cache_25_gb300 import binding as pa
@@ -265,30 +445,21 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     assert pa.pa_get_device_error() == 0
 
+    # launches of this library per step: cache write, decode, the split-K
+    # reduce when some sequence spans several partitions, the chunked prefill
     launches_per_step = 2 + (1 if st.workspace is not None else 0) + (1 if st.R else 0)
-    for _ in range(max(args.warmup, 3)):
+    warmup = max(args.warmup, 3)
+    for _ in range(warmup):
         st.step()
     torch.cuda.synchronize(dev)
 
     # ---- device-timed region: inputs resident in HBM ---------------------
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)] if st.R else [None] * args.steps
-    for a, b in ev:            # torch creates the CUDA event at its first record
-        a.record(stream)
-        b.record(stream)
-    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # A pool that fits in L2 twice over would be read from L2 in steady state:
-    # then every timed step is preceded by a write of a 2 x L2 buffer, outside
-    # the step's own events, and the step time is the mean of those events.
-    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool_bytes = st.k_cache.numel() * st.k_cache.element_size() * 2
-    flush = None
-    if pool_bytes < 2 * l2_bytes:
-        flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
-    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)] if flush is not None else None
+    # K steps back to back between two events on the step's stream; with a
+    # pool small enough to sit in L2, each step is preceded by a 2 x L2 write
+    # outside its own events and the time is the sum of the steps' events.
+    flush, l2_bytes, pool_bytes = _flush_buffer(st, dev)
+    t_start, t_stop = _ev(), _ev()
+    sev = [(_ev(), _ev()) for _ in range(args.steps)] if flush is not None else None
     vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     phys = int(vis[local_rank]) if len(vis) > local_rank and vis[local_rank].strip().isdigit() else local_rank
     clocks = ClockSampler(phys)
@@ -297,26 +468,29 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)   # let the sampler start before the timed region
-    t_start.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            flush.fill_(i & 0xFF)
-            sev[i][0].record(stream)
-        pa.pa_set_profile_events(*ev[i])
-        st.step(prefill_events=pev[i])
-        if flush is not None:
-            sev[i][1].record(stream)
-    t_stop.record(stream)
-    torch.cuda.synchronize(dev)
-    pa.pa_set_profile_events(None, None)
+    with _nvtx("timed steps"):
+        t_start.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+                sev[i][0].record(stream)
+            st.step()
+            if flush is not None:
+                sev[i][1].record(stream)
+        t_stop.record(stream)
+        torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     assert pa.pa_get_device_error() == 0
     ms_total = (t_start.elapsed_time(t_stop) if flush is None else
                 sum(a.elapsed_time(b) for a, b in sev))
-    decode_ms = [a.elapsed_time(b) for a, b in ev]
-    prefill_ms = [a.elapsed_time(b) for a, b in pev] if st.R else None
+
+    # ---- the decode kernel (and the step) per launch, in a loop of its own -
+    n_prof = max(args.steps, args.kernel_steps)
+    with _nvtx("kernel timing"):
+        step_ms, decode_ms, prefill_ms = profiled_steps(st, stream, n_prof, flush)
+    assert pa.pa_get_device_error() == 0
 
     # ---- end to end through the public API with host buffers --------------
     # Every step uploads its inputs from pinned host memory and reads its
@@ -388,29 +562,29 @@ def run_ours(args, rank, world, local_rank):
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize(dev)
-    if flush is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        copy.wait_stream(stream)
-        back.wait_stream(stream)
-        for i in range(e2e_steps):
-            e2e_step(i)
-        stream.wait_stream(back)        # the last read-back is inside the timed region
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        e2e_mode = "pipelined: uploads and read-backs on two copy streams, double-buffered"
-    else:   # a flush between steps: one step at a time
-        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(e2e_steps)]
-        for i in range(e2e_steps):
-            flush.fill_(i & 0xFF)
-            eev[i][0].record(stream)
-            e2e_serial()
-            eev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / e2e_steps
-        e2e_mode = "serial: upload, step, read-back per flushed step"
+    with _nvtx("end to end"):
+        if flush is None:
+            e0, e1 = _ev(), _ev()
+            e0.record(stream)
+            copy.wait_stream(stream)
+            back.wait_stream(stream)
+            for i in range(e2e_steps):
+                e2e_step(i)
+            stream.wait_stream(back)        # the last read-back is inside the timed region
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_ms = e0.elapsed_time(e1) / e2e_steps
+            e2e_mode = "pipelined: uploads and read-backs on two copy streams, double-buffered"
+        else:   # a flush between steps: one step at a time
+            eev = [(_ev(), _ev()) for _ in range(e2e_steps)]
+            for i in range(e2e_steps):
+                flush.fill_(i & 0xFF)
+                eev[i][0].record(stream)
+                e2e_serial()
+                eev[i][1].record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / e2e_steps
+            e2e_mode = "serial: upload, step, read-back per flushed step"
 
     # ---- reductions over ranks (max time) --------------------------------
     ms_step = ms_total / args.steps
@@ -418,39 +592,36 @@ def run_ours(args, rank, world, local_rank):
     ms_step, e2e_ms, dec_ms = max_over_ranks([ms_step, e2e_ms, dec_ms], dev)
 
     kv_unique = st.kv_bytes_unique()
-    kv_logical = st.kv_bytes_logical()
     value = whole_job_gbs(kv_unique, world, ms_step)
     peak, peak_kind = _peaks()
     # algorithmic bytes of the main decode kernel per launch: the unique K/V
-    # bytes plus q, the output/partials are < 0.5% and not counted
+    # bytes (q, the output and the partials are < 0.5 % and not counted)
     achieved = kv_unique / (dec_ms * 1e-3) / 1e9
-    src = _src_hash(DECODE_SOURCES)
-    tr = NCU_TRAFFIC.get((wl.name, B, src))
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3 K/V, f16 products" if wl.cache_dtype is not None else
-                  {"torch.bfloat16": "bf16", "torch.float16": "f16", "torch.float32": "f32"}[str(wl.dtype)]),
+        "dtype": _dtype_name(wl),
         "data": "synthetic (seeded N(0,1) K/V/Q, random block scatter)",
         "config": {"workload": wl.name, "batch": B, "n_q_heads": wl.n_q_heads,
                    "n_kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "num_blocks": st.num_blocks,
                    "prefill_requests": st.R, "q_per_seq": wl.q_per_seq,
                    "parallelism": f"replicas x{world}",
-                   "l2": (f"inputs larger than L2 ({pool_bytes / 1e9:.2f} GB pool, "
-                          f"{kv_unique / 1e9:.2f} GB of K/V read per step); no flush"
-                          if flush is None else
-                          f"L2 flushed before every timed step (a {2 * l2_bytes >> 20} MiB write, "
-                          "outside the step's events); the pool "
-                          f"({pool_bytes / 1e6:.0f} MB) would fit in L2")},
+                   "l2": _l2_note(flush, l2_bytes, pool_bytes, kv_unique)},
         "decode_tokens_per_s": world * B * wl.q_per_seq / (ms_step * 1e-3),
         "steps_per_s": 1e3 / ms_step,
         "pct_of_hbm_peak": 100.0 * value / world / peak,
-        "kv_bytes_unique_per_step": kv_unique, "kv_bytes_logical_per_step": kv_logical,
+        "kv_bytes_unique_per_step": kv_unique,
+        "kv_bytes_block_granular_per_step": st.kv_bytes_block_granular(),
+        "kv_bytes_logical_per_step": st.kv_bytes_logical(),
+        "ms_per_step_median": statistics.median(step_ms),
         "decode_kernel_ms": dec_ms,
+        "decode_kernel_ms_median": statistics.median(decode_ms),
+        "kernel_timing": (f"{n_prof} steps after the timed region, each step and the decode "
+                          "kernel bracketed by CUDA events on the step's stream"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": tr,
+                     "frac": achieved / peak, "traffic": _traffic(wl.name, B),
                      "kernel": "decode_mma_kernel", "peak_source": f"hbm_gbs ({peak_kind})"},
         "e2e": {"value": whole_job_gbs(kv_unique, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -459,36 +630,25 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     if st.R:
-        # inside the step the prefill shares SMs with the decode launched beside
-        # it, so its roofline is taken from the kernel alone: the same call,
-        # timed with events on its own, after the step's timed region
-        alone = []
-        for i in range(max(20, min(args.steps, 100)) + 3):
-            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_.record(stream)
-            pa.pa_prefill_chunk(st.p_out, st.p_q_dev, st.k_cache, st.v_cache, st.p_block_tables,
-                                st.query_start_loc, st.p_context_lens, int(st.p_chunk.max()),
-                                wl.scale, wl.block_size, stream=stream, **st.kv_scales)
-            b_.record(stream)
-            if i >= 3:
-                alone.append((a_, b_))
-        torch.cuda.synchronize(dev)
-        pf_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in alone)
-        flops = st.prefill_flops()
-        tf = _peaks_tensor()
-        line["prefill_flops_per_step"] = flops
-        line["prefill_kernel_ms"] = pf_ms
+        alone = prefill_alone_ms(st, stream, max(20, min(args.steps, 100)))
+        line["prefill_flops_per_step"], line["roofline_prefill"] = _prefill_roofline(st, alone)
         line["prefill_kernel_ms_in_step"] = statistics.mean(prefill_ms)
-        line["roofline_prefill"] = {
-            "bound": "tensor", "achieved": flops / (pf_ms * 1e-3) / 1e12, "peak": tf[0],
-            "unit": "TFLOP/s", "frac": flops / (pf_ms * 1e-3) / 1e12 / tf[0], "traffic": None,
-            "kernel": "prefill_tc_kernel", "peak_source": tf[1],
-            "timing": "kernel alone (in the step it overlaps the decode)"}
         line["prefill_tokens_per_s"] = world * int(st.p_chunk.sum()) / (ms_step * 1e-3)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, t, desc, threads, _ = oracle_sample(wl.name, None, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": desc, "seconds": t}
+    if world == 1 and args.workloads != "none":
+        del st, sets, dev_in, dev_out
+        torch.cuda.empty_cache()
+        names = (OTHER_WORKLOADS if args.workloads == "all" else
+                 tuple(n for n in args.workloads.split(",") if n))
+        recs = []
+        for name in names:
+            if name == wl.name:
+                continue
+            recs.append(measure_workload(name, dev, phys))
+        line["workloads"] = recs
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -507,6 +667,11 @@ def main():
                     help="size the pool at 1.5x the blocks needed (profiling a smaller case)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's decode batch (profiling a smaller case)")
+    ap.add_argument("--kernel-steps", type=int, default=200,
+                    help="steps of the per-launch timing loop after the timed region")
+    ap.add_argument("--workloads", default="all",
+                    help="'all' (every other configuration, one record each, one GPU only), "
+                         "'none', or a comma-separated list of workload names")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

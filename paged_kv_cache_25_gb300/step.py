@@ -14,7 +14,10 @@ several query rows), and run the chunked-prefill requests, if any
 """
 from __future__ import annotations
 
+import collections
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -25,6 +28,22 @@ from .inputs import Draws, Workload
 
 def _ceil_div(a, b):
     return -(-a // b)
+
+
+def _draw_threads() -> int:
+    return max(1, min(16, len(os.sched_getaffinity(0))))
+
+
+def _ordered_window(ex, fn, items, window):
+    """fn(item) for every item, in order, at most `window` results ahead."""
+    items = list(items)
+    pending = collections.deque()
+    for i, it in enumerate(items):
+        pending.append(ex.submit(fn, it))
+        if len(pending) > window:
+            yield pending.popleft().result()
+    while pending:
+        yield pending.popleft().result()
 
 
 class PagedStep:
@@ -84,12 +103,10 @@ class PagedStep:
         # ---- per-step inputs ------------------------------------------------
         B, nq = wl.batch, wl.q_per_seq
         self.q = dr.q().to(dev)
-        new_k = torch.empty((B * nq, n_kv, d), dtype=wl.dtype)
-        new_v = torch.empty((B * nq, n_kv, d), dtype=wl.dtype)
-        prefix = dr.prefix_kv() if self.prefix else None
-        for s in range(B):   # the newest row(s) of every decode sequence
-            k, v = dr.seq_kv(s, int(self.lens[s]), bool(self.sharers[s]), prefix)
-            new_k[s * nq:(s + 1) * nq], new_v[s * nq:(s + 1) * nq] = k[-nq:], v[-nq:]
+        # the newest row(s) of every decode sequence, kept aside by the pre-fill
+        new_k = torch.cat([k for k, _ in self._newest])
+        new_v = torch.cat([v for _, v in self._newest])
+        del self._newest
         seq = np.repeat(np.arange(B, dtype=np.int32), nq)
         pos = (self.lens[:, None] - nq + np.arange(nq)[None, :]).reshape(-1).astype(np.int32)
         slots = pa.pa_slot_mapping(self.tables, bs, seq, pos)
@@ -129,6 +146,7 @@ class PagedStep:
         prefix = dr.prefix_kv() if self.prefix else None
         pending_k, pending_v, pending_s, n = [], [], [], 0
         first_sharer_done = False
+        self._newest = []
 
         def flush():
             nonlocal pending_k, pending_v, pending_s, n
@@ -152,18 +170,22 @@ class PagedStep:
             if n >= chunk_tokens:
                 flush()
 
-        for s in range(wl.batch):
-            L = int(self.lens[s])
-            k, v = dr.seq_kv(s, L, bool(self.sharers[s]), prefix)
-            start = 0
-            if self.sharers[s]:
-                if first_sharer_done:
-                    start = self.prefix           # the shared blocks are written once
-                first_sharer_done = True
-            add(k, v, self.tables, s, start, L - wl.q_per_seq)
-        for r in range(self.R):
-            k, v = dr.prefill_kv(r, int(self.p_lens[r]))
-            add(k, v, self.p_tables, r, 0, int(self.p_ctx[r]))
+        # the draws are keyed per sequence, so worker threads produce them (numpy
+        # and torch release the GIL while filling) in order, a window ahead
+        draw = lambda s: dr.seq_kv(s, int(self.lens[s]), bool(self.sharers[s]), prefix)
+        with ThreadPoolExecutor(_draw_threads()) as ex:
+            for s, (k, v) in enumerate(_ordered_window(ex, draw, range(wl.batch), 32)):
+                L = int(self.lens[s])
+                start = 0
+                if self.sharers[s]:
+                    if first_sharer_done:
+                        start = self.prefix       # the shared blocks are written once
+                    first_sharer_done = True
+                add(k, v, self.tables, s, start, L - wl.q_per_seq)
+                self._newest.append((k[L - wl.q_per_seq:].clone(), v[L - wl.q_per_seq:].clone()))
+            pdraw = lambda r: dr.prefill_kv(r, int(self.p_lens[r]))
+            for r, (k, v) in enumerate(_ordered_window(ex, pdraw, range(self.R), 4)):
+                add(k, v, self.p_tables, r, 0, int(self.p_ctx[r]))
         flush()
 
     def _write(self, k, v, slots, stream=None):
@@ -233,6 +255,16 @@ class PagedStep:
                 b = int(self.tables[s, i])
                 seen[b] = max(seen.get(b, 0), min(bs, int(L) - i * bs))
         return sum(seen.values()) * row
+
+    def kv_bytes_block_granular(self) -> int:
+        """K+V bytes of whole blocks: every distinct physical block the decode
+        touches counted with all block_size rows (masked tail rows included)."""
+        wl, bs = self.wl, self.wl.block_size
+        row = 2 * wl.n_kv_heads * wl.head_dim * wl.pool_elem_bytes
+        blocks = set()
+        for s, L in enumerate(self.lens):
+            blocks.update(int(b) for b in self.tables[s, :_ceil_div(int(L), bs)])
+        return len(blocks) * bs * row
 
     def kv_bytes_logical(self) -> int:
         wl = self.wl
