@@ -278,6 +278,10 @@ def profiled_steps(st, stream, n, flush=None):
     ev = [(_ev(), _ev()) for _ in range(n)]
     dk = [(_ev(), _ev()) for _ in range(n)]
     pf = [(_ev(), _ev()) for _ in range(n)] if st.R else [None] * n
+    for a, b in dk:     # torch creates a CUDA event at its first record; the library
+        a.record(stream)    # records these handles itself, so they must exist first
+        b.record(stream)
+    torch.cuda.synchronize()
     for i in range(n):
         if flush is not None:
             flush.fill_(i & 0xFF)

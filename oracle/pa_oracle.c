@@ -211,6 +211,16 @@ double orc_fp8_e4m3_decode(uint8_t code)
     return sign ? -v : v;
 }
 
+/* The 127 non-negative finite code values, in code order (strictly
+ * increasing; a pin checks it), built once from the decoder. */
+static double g_fp8_vals[0x7F];
+static pthread_once_t g_fp8_once = PTHREAD_ONCE_INIT;
+
+static void fp8_build_table(void)
+{
+    for (int c = 0; c <= 0x7E; ++c) g_fp8_vals[c] = orc_fp8_e4m3_decode((uint8_t)c);
+}
+
 uint8_t orc_fp8_e4m3_encode(float xf)
 {
     double x = (double)xf;
@@ -218,25 +228,46 @@ uint8_t orc_fp8_e4m3_encode(float xf)
     uint8_t sign = signbit(x) ? 0x80 : 0x00;           /* the sign bit, so -0.0 -> 0x80 */
     double a = fabs(x);
     if (a >= 448.0) return (uint8_t)(sign | 0x7E);        /* saturate */
-    /* nearest of the 127 non-negative finite codes, ties to the even code */
-    int best = 0;
-    double best_d = INFINITY;
-    for (int c = 0; c <= 0x7E; ++c) {
-        double d = fabs(orc_fp8_e4m3_decode((uint8_t)c) - a);
-        if (d < best_d || (d == best_d && (c & 1) == 0)) {
-            best = c;
-            best_d = d;
-        }
+    /* nearest of the 127 non-negative finite codes, ties to the even code:
+     * the two codes around a (vals[lo] <= a < vals[lo + 1]) by bisection over
+     * the increasing values, then the nearer of the two */
+    pthread_once(&g_fp8_once, fp8_build_table);
+    int lo = 0, hi = 0x7E;                                /* vals[lo] <= a < vals[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (g_fp8_vals[mid] <= a) lo = mid; else hi = mid;
     }
+    double d_lo = a - g_fp8_vals[lo], d_hi = g_fp8_vals[hi] - a;
+    int best = d_lo < d_hi ? lo : (d_hi < d_lo ? hi : ((lo & 1) == 0 ? lo : hi));
     return (uint8_t)(sign | best);
+}
+
+typedef struct { const float* x; int64_t b, e; float scale; uint8_t* out; } q_job_t;
+
+static void* quantize_worker(void* arg)
+{
+    q_job_t* j = (q_job_t*)arg;
+    for (int64_t i = j->b; i < j->e; ++i) {
+        float q = j->x[i] / j->scale;                      /* fp32 division */
+        j->out[i] = orc_fp8_e4m3_encode(q);
+    }
+    return NULL;
 }
 
 void orc_quantize_fp8(const float* x, int64_t n, float scale, uint8_t* out)
 {
-    for (int64_t i = 0; i < n; ++i) {
-        float q = x[i] / scale;                            /* fp32 division */
-        out[i] = orc_fp8_e4m3_encode(q);
+    /* element-wise, so the work is split in contiguous ranges over threads */
+    int nt = n >= (1 << 20) ? 16 : 1;
+    pthread_t th[16];
+    q_job_t jobs[16];
+    for (int t = 0; t < nt; ++t) {
+        jobs[t].x = x; jobs[t].scale = scale; jobs[t].out = out;
+        jobs[t].b = n * t / nt; jobs[t].e = n * (t + 1) / nt;
+        if (nt == 1) quantize_worker(&jobs[t]);
+        else pthread_create(&th[t], NULL, quantize_worker, &jobs[t]);
     }
+    if (nt > 1)
+        for (int t = 0; t < nt; ++t) pthread_join(th[t], NULL);
 }
 
 void orc_dequantize_fp8(const uint8_t* code, int64_t n, double scale, double* out)

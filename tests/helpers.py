@@ -50,15 +50,17 @@ def oracle_decode_all(step, chunk: int = 32, threads=None) -> np.ndarray:
     sequences at a time (bounded host memory at full workload sizes):
     [B][n_q][d], or [B][q_per_seq][n_q][d] for several query rows per
     sequence (query i at position L - q_per_seq + i, causal among the rows)."""
+    from concurrent.futures import ThreadPoolExecutor
     dr, wl = step.draws, step.wl
     prefix = dr.prefix_kv() if step.prefix else None
     q = dr.q()
     outs = []
+    draw = lambda s: dr.seq_kv(s, int(step.lens[s]), bool(step.sharers[s]), prefix)
+    ex = ThreadPoolExecutor(8)
     for s0 in range(0, wl.batch, chunk):
         seqs = range(s0, min(wl.batch, s0 + chunk))
         ks, vs = [], []
-        for s in seqs:
-            k, v = dr.seq_kv(s, int(step.lens[s]), bool(step.sharers[s]), prefix)
+        for k, v in ex.map(draw, seqs):      # seeded per sequence: order-independent
             k, v = stored_kv(wl, k, v)
             ks.append(k); vs.append(v)
         if wl.q_per_seq == 1:
@@ -66,6 +68,7 @@ def oracle_decode_all(step, chunk: int = 32, threads=None) -> np.ndarray:
         else:
             outs.append(np.stack(oracle.prefill([q[s] for s in seqs], ks, vs, wl.scale,
                                                 threads=threads)))
+    ex.shutdown()
     return np.concatenate(outs)
 
 
