@@ -436,9 +436,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
-        // Descriptors are built once; each MMA only adds a constant to the
-        // start-address field (16-byte units; every operand lies below 256 KB).
-        if (lane == 0) {
+        // The whole warp runs the issue loop (warp-uniform descriptors; one
+        // elected lane issues each MMA and commit).  Descriptors are built once;
+        // each MMA only adds a constant to the start-address field (16-byte
+        // units; every operand lies below 256 KB).
+        {
             const uint64_t dq = sdesc_sw128(sbase + Ly::kOffQ, 16, 1024);
             const uint64_t dk = sdesc_sw128(sbase + Ly::kOffK, 16, 1024);
             // V: MN-major [keys][d] halves (16-bit pools) or K-major [d][keys] halves (FP8)
@@ -456,9 +458,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
                     const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
-                    umma_f16(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
+                    umma_f16_elect(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(smem_u32(&s_full[t]));
+                umma_commit_elect(smem_u32(&s_full[t]));
             };
             // O_t += P_t(j) V_j, P from TMEM (hi and lo halves of each 16 keys)
             auto issue_pv = [&](int t, int j) {
@@ -475,28 +477,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     // 32 B into a 64-key half of the [d][keys] tile (K-major)
                     const uint32_t vst = F8 ? (ks >> 2) * ((D * 128) >> 4) + (ks & 3) * 2
                                             : ks * (2048 >> 4);
-                    umma_f16_ts(d_o, a_p + col, dvs + vst, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-                    umma_f16_ts(d_o, a_p + col + 16, dvs + vst, kIdescPV, 1u);
+                    umma_f16_ts_elect(d_o, a_p + col, dvs + vst, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16_ts_elect(d_o, a_p + col + 16, dvs + vst, kIdescPV, 1u);
                 }
-                umma_commit(smem_u32(&pv_done[t]));
+                umma_commit_elect(smem_u32(&pv_done[t]));
             };
-            bool ok = mbar_wait(smem_u32(&q_ready), 0, err) &&
-                      mbar_wait(smem_u32(&k_full[0]), 0, err);
+            // every lane polls; the warp goes on only if all saw the phase
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, err));
+            };
+            bool ok = wait_all(&q_ready, 0) && wait_all(&k_full[0], 0);
             tc_fence_after();
             if (ok) {
                 for (int t = 0; t < kTcTiles; ++t)
                     if (n_t[t] > 0) issue_qk(t, 0);
-                umma_commit(smem_u32(&k_empty[0]));
+                umma_commit_elect(smem_u32(&k_empty[0]));
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % kTcStages, st1 = (j + 1) % kTcStages;
                 const bool more = j + 1 < n_tiles;
-                if (!mbar_wait(smem_u32(&v_full[st]), (j / kTcStages) & 1, err)) break;
-                if (more && !mbar_wait(smem_u32(&k_full[st1]), ((j + 1) / kTcStages) & 1, err)) break;
+                if (!wait_all(&v_full[st], (j / kTcStages) & 1)) break;
+                if (more && !wait_all(&k_full[st1], ((j + 1) / kTcStages) & 1)) break;
 #pragma unroll
                 for (int t = 0; t < kTcTiles; ++t) {
                     if (j >= n_t[t]) continue;
-                    if (!mbar_wait(smem_u32(&p_full[t]), j & 1, err)) {
+                    if (!wait_all(&p_full[t], j & 1)) {
                         ok = false;
                         break;
                     }
@@ -505,8 +510,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     if (j + 1 < n_t[t]) issue_qk(t, j + 1);
                 }
                 if (!ok) break;
-                umma_commit(smem_u32(&v_empty[st]));
-                if (more) umma_commit(smem_u32(&k_empty[st1]));
+                umma_commit_elect(smem_u32(&v_empty[st]));
+                if (more) umma_commit_elect(smem_u32(&k_empty[st1]));
             }
         }
     } else {
