@@ -268,11 +268,28 @@ def _l2_note(flush, l2_bytes, pool_bytes, kv_unique):
             f"the step's events); the pool ({pool_bytes / 1e6:.0f} MB) would fit in L2")
 
 
+def timed_steps(st, stream, n, flush=None):
+    """n steps, each bracketed by a pair of CUDA events on the step's stream
+    and nothing else between its kernels (the L2 flush, if any, goes before
+    the first event).  Returns the per-step times in ms."""
+    import torch
+    ev = [(_ev(), _ev()) for _ in range(n)]
+    for i in range(n):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        st.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def profiled_steps(st, stream, n, flush=None):
     """n steps, each bracketed by CUDA events on the step's stream, the decode
     kernel by the library's profiling events and the chunked prefill (if any)
     by events on its side stream.  Returns per-step lists in ms: step, decode
-    kernel, prefill kernel (inside the step)."""
+    kernel, prefill kernel (inside the step).  The events recorded between the
+    step's kernels serialise them, so step times come from timed_steps."""
     import torch
     from paged_kv_cache_25_gb300 import binding as pa
     ev = [(_ev(), _ev()) for _ in range(n)]
@@ -357,14 +374,16 @@ def measure_workload(name, dev, phys, target_s=0.6, min_steps=50, max_steps=3000
     for _ in range(10):
         st.step()
     torch.cuda.synchronize(dev)
-    probe, _, _ = profiled_steps(st, stream, 5, flush)
+    probe = timed_steps(st, stream, 5, flush)
     n = int(min(max_steps, max(min_steps, target_s / max(statistics.median(probe), 1e-3) * 1e3)))
     clocks = ClockSampler(phys)
     clocks.start()
     time.sleep(0.3)
     with _nvtx(f"workload {name}"):
-        step_ms, dec_ms, pf_ms = profiled_steps(st, stream, n, flush)
+        step_ms = timed_steps(st, stream, n, flush)
     clk = clocks.stop()
+    with _nvtx(f"workload {name} kernels"):
+        _, dec_ms, pf_ms = profiled_steps(st, stream, min(n, 500), flush)
     assert pa.pa_get_device_error() == 0
     kv_unique = st.kv_bytes_unique()
     peak, peak_kind = _peaks()
@@ -490,10 +509,13 @@ def run_ours(args, rank, world, local_rank):
     ms_total = (t_start.elapsed_time(t_stop) if flush is None else
                 sum(a.elapsed_time(b) for a, b in sev))
 
-    # ---- the decode kernel (and the step) per launch, in a loop of its own -
+    # ---- per-step times (median) and the decode kernel per launch, in loops of
+    # their own after the timed region
     n_prof = max(args.steps, args.kernel_steps)
+    with _nvtx("step times"):
+        step_ms = timed_steps(st, stream, n_prof, flush)
     with _nvtx("kernel timing"):
-        step_ms, decode_ms, prefill_ms = profiled_steps(st, stream, n_prof, flush)
+        _, decode_ms, prefill_ms = profiled_steps(st, stream, n_prof, flush)
     assert pa.pa_get_device_error() == 0
 
     # ---- end to end through the public API with host buffers --------------
@@ -622,8 +644,9 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step_median": statistics.median(step_ms),
         "decode_kernel_ms": dec_ms,
         "decode_kernel_ms_median": statistics.median(decode_ms),
-        "kernel_timing": (f"{n_prof} steps after the timed region, each step and the decode "
-                          "kernel bracketed by CUDA events on the step's stream"),
+        "kernel_timing": (f"after the timed region: {n_prof} steps each bracketed by CUDA events "
+                          f"(ms_per_step_median), then {n_prof} more with the decode kernel "
+                          "bracketed by events on the step's stream (decode_kernel_ms)"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _traffic(wl.name, B),
                      "kernel": "decode_mma_kernel", "peak_source": f"hbm_gbs ({peak_kind})"},

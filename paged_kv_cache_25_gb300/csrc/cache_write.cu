@@ -18,6 +18,9 @@ cache_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                    const int64_t* __restrict__ slots, int64_t total, int n_kv, int block_size,
                    int chunks_per_row, int64_t num_slots, unsigned* err)
 {
+    // the decode launched next (a programmatic dependent) may be scheduled at
+    // once; it waits for this grid to complete before it reads the pool
+    allow_dependent_launch();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= total) return;
     const int64_t row = i / chunks_per_row;       // (token, head) row
@@ -108,6 +111,7 @@ cache_write_fp8_kernel(const TI* __restrict__ k, const TI* __restrict__ v, uint4
                        int n_kv, int block_size, int pieces_per_row, int64_t num_slots,
                        float k_scale, float v_scale, unsigned* err)
 {
+    allow_dependent_launch();   // as in cache_write_kernel
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= total) return;
     const int64_t row = i / pieces_per_row;       // (token, head) row

@@ -93,6 +93,7 @@ decode_reduce_kernel(void* __restrict__ out, pa_dtype out_dtype,
 {
     constexpr int D = DPL * 32;
     const int lane = threadIdx.x & 31;
+    grid_dependency_wait();   // launched as a programmatic dependent of the partial kernel
     // one warp per output row ((sequence, query) x head)
     const int64_t sh = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     if (sh >= static_cast<int64_t>(num_seqs) * nq * n_q) return;
@@ -152,29 +153,35 @@ static cudaError_t run_reduce(const DecodeArgs& a, cudaStream_t s)
 {
     const int64_t pairs = static_cast<int64_t>(a.num_seqs) * a.q_per_seq * a.n_q;
     const unsigned grid = static_cast<unsigned>((pairs + 3) / 4);
-#define PA_REDUCE(DPL)                                                                          \
-    decode_reduce_kernel<DPL><<<grid, 128, 0, s>>>(a.out, a.out_dtype, a.context_lens, a.ws_ml, \
-                                                   a.ws_acc, a.num_seqs, a.n_q, a.q_per_seq,    \
-                                                   a.part_tokens, a.max_parts)
+    // a programmatic dependent of the partial kernel: its launch overlaps that
+    // kernel's tail, and it waits for the partials before reading them
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#define PA_REDUCE(DPL)                                                                            \
+    cudaLaunchKernelEx(&cfg, decode_reduce_kernel<DPL>, a.out, a.out_dtype, a.context_lens,       \
+                       static_cast<const float*>(a.ws_ml), static_cast<const float*>(a.ws_acc),  \
+                       a.num_seqs, a.n_q, a.q_per_seq, a.part_tokens, a.max_parts)
     switch (a.cache.head_dim) {
-        case 32: PA_REDUCE(1); break;
-        case 64: PA_REDUCE(2); break;
-        case 96: PA_REDUCE(3); break;
-        case 128: PA_REDUCE(4); break;
-        case 256: PA_REDUCE(8); break;
+        case 32: return PA_REDUCE(1);
+        case 64: return PA_REDUCE(2);
+        case 96: return PA_REDUCE(3);
+        case 128: return PA_REDUCE(4);
+        case 256: return PA_REDUCE(8);
         default: return cudaErrorInvalidValue;
     }
 #undef PA_REDUCE
-    return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s)
 {
     const float sl2 = a.scale * 1.4426950408889634f;   // softmax in base 2
-    if (a.cache.dtype != PA_F32) {   // the tensor-core kernels take work from a counter
-        cudaError_t e0 = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), s);
-        if (e0 != cudaSuccess) return e0;
-    }
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     profile_events(&ev0, &ev1);
     if (ev0) cudaEventRecord(ev0, s);

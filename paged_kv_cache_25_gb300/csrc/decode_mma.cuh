@@ -66,6 +66,7 @@ constexpr int kSmemPerSm = 233472;    // 228 KB of shared memory per SM
 // 2-stage ring, 9,424 B at d 64 with 6 stages; the prefix table is 8 KB of it)
 constexpr int kStaticSmem = 9728;
 constexpr int kPreferSepRed = 1;      // give the combine its own buffer when it fits
+constexpr int kStaticUnitsPerCta = 4; // batches up to this many units per CTA: round robin
 
 // Dynamic shared memory a CTA may use at the resident count above.
 constexpr int decode_dyn_avail(bool fp8)
@@ -165,6 +166,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                                                ~static_cast<uintptr_t>(1023));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // launched as a programmatic dependent: every input may come from the
+    // kernel before this one in the stream
+    grid_dependency_wait();
     // a KV head serves group x nq rows (head-major: row = head * nq + query),
     // taken RU at a time; plain decode (MQ false) has nq = 1 at compile time
     const int nq = MQ ? nq_arg : 1;
@@ -222,7 +226,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     }
 
     // Units are handed out dynamically: unit blockIdx.x first, then tickets
-    // from a counter that starts at zero for every launch.  Work for the next
+    // from a counter that starts at zero for every launch (or, for batches of
+    // at most a few units per CTA, round robin with no counter).  Work for the next
     // unit overlaps the current one: its ticket is drawn one unit ahead, its
     // block ids are loaded (one per thread) while the current unit streams,
     // its q fragments while the current unit's warps combine, and - when the
@@ -362,7 +367,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (cu.live && tid < cu.nblk) s_blk[0][tid] = load_id(cu, tid, bad);
         load_q(cu);
         const int any_bad = __syncthreads_or(bad);
-        if (tid == 0) s_next = static_cast<long long>(gridDim.x) + atomicAdd(ticket, 1u);
+        if (tid == 0)
+            s_next = ticket ? static_cast<long long>(gridDim.x) + atomicAdd(ticket, 1u)
+                            : u + static_cast<long long>(gridDim.x);
         cu.live = cu.live && !any_bad;
         __syncthreads();
     }
@@ -648,7 +655,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // every ring is idle and (separate buffer) the partials are written
         const int flags = __syncthreads_or(timed_out | (nb_bad << 1));
         if (flags & 1) return;
-        if (tid == 0) s_next = static_cast<long long>(gridDim.x) + atomicAdd(ticket, 1u);
+        if (tid == 0)
+            s_next = ticket ? static_cast<long long>(gridDim.x) + atomicAdd(ticket, 1u)
+                            : un + static_cast<long long>(gridDim.x);
+        // this CTA's last unit: the kernel after this one may be scheduled now
+        if (un >= units) allow_dependent_launch();
         const bool next_live = nx.live && !(flags & 2);
         if (cu.live) {
             if constexpr (!Cfg::kSepRed) {
@@ -786,13 +797,32 @@ cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
                           ((group * a.q_per_seq + RU - 1) / RU);
     const int64_t resident = static_cast<int64_t>(decode_sm_count()) * per_sm;
     const unsigned grid = static_cast<unsigned>(upper < resident ? upper : resident);
-    kern<<<grid, kDecWarps * 32, Cfg::kDynBytes, s>>>(
-        kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
-        a.context_lens, a.num_seqs, a.n_q, a.q_per_seq, a.cache.n_kv_heads, group,
-        a.cache.num_blocks,
-        FP8 ? scale_log2 * a.cache.k_scale : scale_log2, FP8 ? a.cache.v_scale : 1.f, a.ws_ml,
-        a.ws_acc, a.part_tokens, a.max_parts, a.ticket, a.err);
-    return cudaGetLastError();
+    // small batches (at most kStaticUnitsPerCta units per resident CTA, counted
+    // with every sequence at the longest length) are dealt round robin: no
+    // counter to clear, so no memset before the launch
+    unsigned* ticket = upper <= kStaticUnitsPerCta * resident ? nullptr : a.ticket;
+    if (ticket) {
+        const cudaError_t e0 = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
+        if (e0 != cudaSuccess) return e0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecWarps * 32);
+    cfg.dynamicSmemBytes = Cfg::kDynBytes;
+    cfg.stream = s;
+    // with no memset in front, the kernel is a programmatic dependent of the
+    // kernel before it (the cache write): it is scheduled while that one
+    // drains and waits for it before reading any input
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ticket ? 0 : 1;
+    return cudaLaunchKernelEx(
+        &cfg, kern, kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables,
+        a.max_blocks, a.context_lens, a.num_seqs, a.n_q, a.q_per_seq, a.cache.n_kv_heads, group,
+        a.cache.num_blocks, FP8 ? scale_log2 * a.cache.k_scale : scale_log2,
+        FP8 ? a.cache.v_scale : 1.f, a.ws_ml, a.ws_acc, a.part_tokens, a.max_parts, ticket, a.err);
 }
 
 // Tensor-core kernels by shape; cudaErrorNotSupported for other shapes.

@@ -104,6 +104,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// ----------------------------------------------------------------- dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// kernel before it in the stream finishes; it waits here, before reading any
+// memory that earlier stream work may write, until that work has completed
+// and its writes are visible.  (A no-op for an ordinary launch.)
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel of the stream, if it was launched with programmatic
+// stream serialization, be scheduled now (it still waits for this grid's
+// completion before its reads; see grid_dependency_wait).
+__device__ __forceinline__ void allow_dependent_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- TMA
 // 2-D tiled load of box {x extent, y extent} at coordinates (x, y) into smem,
 // completing on the mbarrier with the transaction byte count.

@@ -53,7 +53,8 @@ struct DecodeArgs {
     float* ws_acc;     // [B][q_per_seq][n_q][J][d] or null
     int part_tokens;   // tokens per partition
     int max_parts;     // J: partitions of the longest possible sequence
-    unsigned* ticket;  // work counter in the workspace's control area
+    unsigned* ticket;  // work counter in the workspace's control area; null: units are
+                       // dealt round robin (unit blockIdx.x + k * gridDim.x), no counter
     unsigned* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
