@@ -36,17 +36,22 @@ METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode tokens/s"
 DEFAULT_WORKLOAD = "llama3-8b-bf16"
 FALLBACK_HBM_GBS = 6800.0
 
-# ncu DRAM traffic of the main decode kernel on this workload, per launch
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel
-# sources are byte-identical to what was profiled (sha256 of DECODE_SOURCES).
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch,
+# valid only while the kernel sources are byte-identical to what was profiled
+# (sha256 prefix of DECODE_SOURCES / PREFILL_SOURCES).  Decode: (bytes, unique
+# K/V bytes of the captured launch, what was captured); a record of another
+# batch of the same workload is scaled by its unique K/V bytes.
 NCU_TRAFFIC = {
-    # one-pass ncu captures (--metrics dram__bytes_read.sum,dram__bytes_write.sum
-    # of the decode kernel, 4th launch)
-    ("llama3-8b-bf16", 256, "ad80b383e235384f"): 2371977216 + 13616640,
-    ("llama3-8b-fp8", 256, "ad80b383e235384f"): 1188184576 + 12948224,
-    ("llama3-8b-bf16-verify4", 256, "ad80b383e235384f"): 2384849152 + 44538624,
-    ("opt13b-fp16", 128, "ad80b383e235384f"): 5371655936 + 8389376,
-    ("mixed-llama3-8b-bf16", 192, "ad80b383e235384f"): 1446247936 + 9858304,
+    ("llama3-8b-bf16", "222c6a85c05167fc"): (2371994368 + 13491712, 2359717888,
+                                             "full 256-sequence batch, one-pass capture"),
+    ("llama3-8b-fp8", "222c6a85c05167fc"): (311070720 + 4660736, 308879360,
+                                            "64-sequence batch (--set full), scaled by unique K/V bytes"),
+}
+# chunked prefill of the mixed step (the compact-pool capture runs the same four
+# chunks as the 60 GB pool): bytes per launch
+NCU_PREFILL_TRAFFIC = {
+    ("mixed-llama3-8b-bf16", "ac86ec92b3feb147"): (98359552 + 5173248, "compact pool, --set full"),
+    ("mixed-llama3-8b-fp8", "ac86ec92b3feb147"): (57597184 + 1532160, "compact pool, --set full"),
 }
 
 
@@ -72,8 +77,9 @@ def _peaks_tensor():
         return 1700.0, "bf16 sustained (fallback)"
 
 
-# the decode kernel's sources: traffic figures hold only while these are unchanged
+# the kernels' sources: traffic figures hold only while these are unchanged
 DECODE_SOURCES = ("decode_mma.cuh", "decode.cu", "decode_verify.cu", "pa_device.cuh")
+PREFILL_SOURCES = ("prefill_tc.cu", "pa_device.cuh")
 
 
 def _src_hash(names) -> str:
@@ -340,18 +346,29 @@ def _dtype_name(wl):
     return {"torch.bfloat16": "bf16", "torch.float16": "f16", "torch.float32": "f32"}[str(wl.dtype)]
 
 
-def _traffic(name, batch):
-    src = _src_hash(DECODE_SOURCES)
-    return NCU_TRAFFIC.get((name, batch, src))
+def _traffic(name, kv_unique):
+    """(bytes per launch, how it was obtained) or (None, reason)."""
+    rec = NCU_TRAFFIC.get((name, _src_hash(DECODE_SOURCES)))
+    if rec is None:
+        return None, "no ncu capture of the current decode sources on this workload"
+    b, u, how = rec
+    return int(round(b * kv_unique / u)), how
+
+
+def _prefill_traffic(name):
+    rec = NCU_PREFILL_TRAFFIC.get((name, _src_hash(PREFILL_SOURCES)))
+    return (rec[0], rec[1]) if rec else (None, "no ncu capture of the current prefill sources")
 
 
 def _prefill_roofline(st, pf_ms):
     flops = st.prefill_flops()
     tf, tf_src = _peaks_tensor()
     achieved = flops / (statistics.mean(pf_ms) * 1e-3) / 1e12
+    traffic, how = _prefill_traffic(st.wl.name)
     return flops, {
         "bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s",
-        "frac": achieved / tf, "traffic": None, "kernel": "prefill_tc_kernel",
+        "frac": achieved / tf, "traffic": traffic, "traffic_source": how,
+        "kernel": "prefill_tc_kernel",
         "peak_source": tf_src, "kernel_ms_mean": statistics.mean(pf_ms),
         "kernel_ms_median": statistics.median(pf_ms), "launches_timed": len(pf_ms),
         "timing": "kernel alone (in the step it overlaps the decode)"}
@@ -404,7 +421,8 @@ def measure_workload(name, dev, phys, target_s=0.6, min_steps=50, max_steps=3000
         "kv_bytes_logical_per_step": st.kv_bytes_logical(),
         "decode_kernel_ms_mean": dmean, "decode_kernel_ms_median": dmed,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _traffic(wl.name, wl.batch),
+                     "frac": achieved / peak, "traffic": _traffic(wl.name, kv_unique)[0],
+                     "traffic_source": _traffic(wl.name, kv_unique)[1],
                      "kernel": "decode_mma_kernel", "peak_source": f"hbm_gbs ({peak_kind})"},
         "l2": _l2_note(flush, l2_bytes, pool_bytes, kv_unique),
         "clocks": clk, "setup_s": setup_s,
@@ -648,7 +666,8 @@ def run_ours(args, rank, world, local_rank):
                           f"(ms_per_step_median), then {n_prof} more with the decode kernel "
                           "bracketed by events on the step's stream (decode_kernel_ms)"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _traffic(wl.name, B),
+                     "frac": achieved / peak, "traffic": _traffic(wl.name, kv_unique)[0],
+                     "traffic_source": _traffic(wl.name, kv_unique)[1],
                      "kernel": "decode_mma_kernel", "peak_source": f"hbm_gbs ({peak_kind})"},
         "e2e": {"value": whole_job_gbs(kv_unique, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
