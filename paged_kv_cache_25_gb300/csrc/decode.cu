@@ -39,32 +39,72 @@ decode_simt_kernel(void* __restrict__ out, pa_dtype out_dtype, const T* __restri
         acc[i] = 0.f;
     }
     float m_run = -INFINITY, l_run = 0.f;
-    int64_t base = 0;
-    for (int p = tok0; p < tok1; ++p) {
-        const int off = p % block_size;
-        if (off == 0 || p == tok0) {
-            const int lb = p / block_size;
-            int b = lb < max_blocks ? __ldg(block_tables + static_cast<int64_t>(s) * max_blocks + lb) : -1;
-            if (b < 0 || b >= num_blocks) {
-                set_error(err, PA_ERR_OUT_OF_RANGE);
-                return;
+    // tokens in groups of kTok: their K/V rows are loaded before any of them is
+    // used, so the loads of a group overlap (one token at a time left every
+    // warp waiting on one row's latency per token)
+    constexpr int kTok = 4;
+    const int32_t* table = block_tables + static_cast<int64_t>(s) * max_blocks;
+    for (int p0 = tok0; p0 < tok1; p0 += kTok) {
+        float kf[kTok][DPL], vf[kTok][DPL];
+        bool bad = false;
+#pragma unroll
+        for (int u = 0; u < kTok; ++u) {
+            const int p = p0 + u;
+            if (p < tok1) {
+                const int lb = p / block_size;
+                const int b = lb < max_blocks ? __ldg(table + lb) : -1;
+                bad = bad || b < 0 || b >= num_blocks;
+                const int64_t row = (static_cast<int64_t>(b < 0 ? 0 : b) * n_kv + kvh) * block_size +
+                                    p % block_size;
+                const T* kr = kc + row * D;
+                const T* vr = vc + row * D;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) {
+                    kf[u][i] = b < 0 || b >= num_blocks ? 0.f : Cvt<T>::to_f(kr[lane + 32 * i]);
+                    vf[u][i] = b < 0 || b >= num_blocks ? 0.f : Cvt<T>::to_f(vr[lane + 32 * i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) kf[u][i] = vf[u][i] = 0.f;
             }
-            base = (static_cast<int64_t>(b) * n_kv + kvh) * block_size;
         }
-        const T* kr = kc + (base + off) * D;
-        const T* vr = vc + (base + off) * D;
-        float dot = 0.f;
+        if (bad) {                 // the same block ids in every lane: uniform
+            set_error(err, PA_ERR_OUT_OF_RANGE);
+            return;
+        }
+        float z[kTok];
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) dot = fmaf(qv[i], Cvt<T>::to_f(kr[lane + 32 * i]), dot);
+        for (int u = 0; u < kTok; ++u) {
+            float dot = 0.f;
 #pragma unroll
-        for (int w = 16; w > 0; w >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, w);
-        const float z = dot * scale_log2;
-        const float m_new = fmaxf(m_run, z);
-        const float alpha = exp2f(m_run - m_new);
-        const float pz = exp2f(z - m_new);
-        l_run = l_run * alpha + pz;
+            for (int i = 0; i < DPL; ++i) dot = fmaf(qv[i], kf[u][i], dot);
+            z[u] = dot;
+        }
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(pz, Cvt<T>::to_f(vr[lane + 32 * i]), acc[i] * alpha);
+        for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+            for (int u = 0; u < kTok; ++u) z[u] += __shfl_xor_sync(0xffffffffu, z[u], w);
+        float m_new = m_run;
+#pragma unroll
+        for (int u = 0; u < kTok; ++u) {
+            z[u] = p0 + u < tok1 ? z[u] * scale_log2 : -INFINITY;
+            m_new = fmaxf(m_new, z[u]);
+        }
+        const float alpha = exp2f(m_run - m_new);   // 0 on the first group (m_run = -inf)
+        float pz[kTok], psum = 0.f;
+#pragma unroll
+        for (int u = 0; u < kTok; ++u) {
+            pz[u] = p0 + u < tok1 ? exp2f(z[u] - m_new) : 0.f;
+            psum += pz[u];
+        }
+        l_run = l_run * alpha + psum;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) {
+            float a = acc[i] * alpha;
+#pragma unroll
+            for (int u = 0; u < kTok; ++u) a = fmaf(pz[u], vf[u][i], a);
+            acc[i] = a;
+        }
         m_run = m_new;
     }
     const int64_t sh = static_cast<int64_t>(s) * n_q + h;

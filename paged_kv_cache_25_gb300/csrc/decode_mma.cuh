@@ -59,8 +59,13 @@ __device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dt
 }
 
 // Resident CTAs per SM: FP8 stages cost the same fragment work for half the
-// bytes, so that path is bound by per-warp latency and runs more warps.
-constexpr int decode_ctas_per_sm(bool fp8) { return fp8 ? 3 : 2; }
+// bytes, so that path is bound by per-warp latency and runs more warps; so do
+// 16-bit pools with head_dim 64 (half the bytes per row, and the register
+// count of those variants fits 3 CTAs of 4 warps).
+constexpr int decode_ctas_per_sm(bool fp8, int D = 128, int RU = 8)
+{
+    return fp8 || (D == 64 && RU == 8) ? 3 : 2;
+}
 constexpr int kSmemPerSm = 233472;    // 228 KB of shared memory per SM
 // bound on the kernel's static shared memory (ptxas: 9,296 B at d 128 with a
 // 2-stage ring, 9,424 B at d 64 with 6 stages; the prefix table is 8 KB of it)
@@ -69,9 +74,10 @@ constexpr int kPreferSepRed = 1;      // give the combine its own buffer when it
 constexpr int kStaticUnitsPerCta = 4; // batches up to this many units per CTA: round robin
 
 // Dynamic shared memory a CTA may use at the resident count above.
-constexpr int decode_dyn_avail(bool fp8)
+constexpr int decode_dyn_avail(bool fp8, int D = 128, int RU = 8)
 {
-    return kSmemPerSm / decode_ctas_per_sm(fp8) - 1024 /* reserved */ - kStaticSmem - 1024 /* align */;
+    return kSmemPerSm / decode_ctas_per_sm(fp8, D, RU) - 1024 /* reserved */ - kStaticSmem -
+           1024 /* align */;
 }
 
 // Ring depth per warp: about `budget` bytes of K+V in flight per warp, at least
@@ -84,7 +90,7 @@ constexpr int decode_stages()
     constexpr int budget = FP8 ? 12288 : 24576;
     constexpr int ns = budget / stage > 2 ? budget / stage : 2;
     constexpr int red = kDecWarps * RU * (D + 2) * 4;
-    constexpr int fit = (decode_dyn_avail(FP8) - red) / (kDecWarps * stage);
+    constexpr int fit = (decode_dyn_avail(FP8, D, RU) - red) / (kDecWarps * stage);
     return kPreferSepRed && fit >= 2 ? (fit < ns ? fit : ns) : ns;
 }
 
@@ -103,7 +109,7 @@ struct DecodeCfg {
     static constexpr int kReduceBytes = kDecWarps * RU * (D + 2) * 4;
     // the combine buffer sits after the rings when both fit, else it aliases them
     static constexpr bool kSepRed =
-        kPreferSepRed && kRingBytes + kReduceBytes <= decode_dyn_avail(FP8);
+        kPreferSepRed && kRingBytes + kReduceBytes <= decode_dyn_avail(FP8, D, RU);
     static constexpr int kRedOffset = kSepRed ? kRingBytes : 0;
     static constexpr int kDynBytes =
         (kSepRed ? kRingBytes + kReduceBytes
@@ -136,7 +142,7 @@ __device__ __forceinline__ uint32_t q_pair<__nv_bfloat16, __half>(const __nv_bfl
 }
 
 template <typename T, typename QT, int D, int BS, int NS, bool FP8, bool MQ, int RU = 8>
-__global__ void __launch_bounds__(kDecWarps * 32, decode_ctas_per_sm(FP8))
+__global__ void __launch_bounds__(kDecWarps * 32, decode_ctas_per_sm(FP8, D, RU))
 decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
