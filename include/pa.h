@@ -130,8 +130,10 @@ pa_status pa_reshape_and_cache_quant(const void* k, const void* v, pa_dtype in_d
  *   workspace    : device scratch of at least pa_decode_workspace_size(...)
  *                  bytes for the same shapes, 256-byte aligned; its contents
  *                  need no initialisation.  It holds the work counter of the
- *                  persistent decode kernel (reset on the stream by each call)
- *                  and, for long contexts split over several thread blocks,
+ *                  persistent decode kernel (reset on the stream by each call
+ *                  that uses one; batches of a few units per resident thread
+ *                  block are dealt round robin and use none) and, for long
+ *                  contexts split over several thread blocks,
  *                  the partial results the second kernel combines.  Calls that
  *                  overlap on the GPU must not share one workspace.
  * n_q_heads must be a multiple of n_kv_heads.  Accumulation is fp32.
@@ -194,9 +196,9 @@ size_t pa_decode_verify_workspace_size(int num_seqs, int q_per_seq, int n_q_head
  *     one-time set-up per device); make that first call before any stream
  *     capture.
  *   - All calls share the array and it keeps the last call's contents; what
- *     must start at zero (the work counter) is cleared on the stream by every
- *     call.  Calls that overlap on the GPU (other streams, other host threads)
- *     race on it: serialise them. */
+ *     must start at zero (the work counter, when the batch uses one) is
+ *     cleared on the stream by every call that uses it.  Calls that overlap on
+ *     the GPU (other streams, other host threads) race on it: serialise them. */
 #define PA_DECODE_NO_ALLOC_SCRATCH_BYTES (16u << 20)
 pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
                              const void* k_cache, const void* v_cache, const pa_cache_desc* cache,

@@ -9,9 +9,9 @@
 //
 // The array lives on every GPU that loads the library, until the process
 // exits.  All calls share it and it keeps the previous call's contents; the
-// one word that must start at zero (the decode's work counter) is cleared on
-// the stream by every call, and every partial the reduce reads is written
-// earlier in the same call.  Calls whose work overlaps on the GPU (different
+// one word that must start at zero (the decode's work counter, for batches
+// large enough to use one) is cleared on the stream by every call that uses
+// it, and every partial the reduce reads is written earlier in the same call.  Calls whose work overlaps on the GPU (different
 // streams, or several host threads) race on it.
 #include <mutex>
 
