@@ -618,18 +618,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             // 2^(s*c - m*c) is one FFMA and one EX2)
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (ok) {
+                uint32_t sa[32], sb[32];       // both loads in flight, one wait
+                tmem_ld32(lane_addr + s_col, sa);
+                tmem_ld32(lane_addr + s_col + 32, sb);
+                tmem_ld_wait();
+                if (full_tile) {
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t sr[32];
-                    tmem_ld32(lane_addr + s_col + h2 * 32, sr);
-                    tmem_ld_wait();
-                    if (full_tile) {
+                    for (int i = 0; i < 32; ++i) {
+                        m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sa[i]));
+                        m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sb[i]));
+                    }
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (hkey0 + h2 * 32 + i <= p_abs) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sr[i]));
+                    for (int i = 0; i < 32; ++i) {
+                        if (hkey0 + i <= p_abs) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sa[i]));
+                        if (hkey0 + 32 + i <= p_abs) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sb[i]));
                     }
                 }
             }
