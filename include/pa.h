@@ -64,7 +64,8 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
  * in {16, 32} run on the tensor-core paths; fp32 pools run on a CUDA-core
  * path.  n_kv_heads >= 1.
  * FP8 pools ("The hands-on guide to LLM Inference with vLLM", KV footprint:
- * 1 byte per element if the cache is quantized to FP8): dtype PA_FP8_E4M3,
+ * 1 byte per element if the cache is quantized to FP8; head_dim 64 or 128):
+ * dtype PA_FP8_E4M3,
  * each stored code c means decode_e4m3(c) * k_scale for K (v_scale for V);
  * act_dtype (PA_BF16 or PA_F16) is the dtype of q and of the K/V rows given
  * to pa_reshape_and_cache_quant.  The three fields are ignored otherwise.

@@ -254,6 +254,8 @@ pa_status pa_reshape_and_cache_quant(const void* k, const void* v, pa_dtype in_d
         (in_dtype != PA_F32 && in_dtype != PA_F16 && in_dtype != PA_BF16))
         return fail(PA_ERR_UNSUPPORTED, "cache write from dtype %d into dtype %d", (int)in_dtype,
                     (int)cache->dtype);
+    if (cache->head_dim != 64 && cache->head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "FP8 pools take head_dim 64 or 128");
     if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
     if (num_tokens == 0) return ok();
     if (!k || !v || !k_cache || !v_cache || !slot_mapping)
@@ -276,6 +278,8 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
 {
     pa_status st = check_cache(cache, false);
     if (st != PA_OK) return st;
+    if (cache->dtype == PA_FP8_E4M3 && cache->head_dim != 64 && cache->head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "FP8 pools take head_dim 64 or 128");
     if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
     if (num_tokens == 0) return ok();
     if (!k || !v || !k_cache || !v_cache || !slot_mapping)

@@ -56,6 +56,42 @@ def test_fp8_cache_write_whole_pool_bit_exact(act, scale):
     assert (ek == 0x80).any() and (ev == 0x80).any()
 
 
+@pytest.mark.parametrize("bs,d", [(16, 128), (32, 64), (32, 128), (16, 64)])
+def test_fp8_cache_write_slot_patterns_bit_exact(bs, d):
+    """Slot patterns the writer stores differently: 16 aligned consecutive slots
+    (whole 16-byte rows of the transposed V slab), aligned runs of 4, an
+    unaligned run, scattered slots, padding (-1) and a ragged tail of tokens.
+    Every byte of both pools equals the oracle's writes of the oracle's codes."""
+    nb, n_kv = 12, 3
+    rng = np.random.default_rng(bs + d)
+    runs = [np.arange(2 * bs, 2 * bs + 16),                 # aligned 16
+            np.arange(5 * bs + 4, 5 * bs + 8),              # aligned 4 ...
+            np.arange(7 * bs + 0, 7 * bs + 4),
+            np.array([3 * bs + 1, 3 * bs + 2, 3 * bs + 3, 3 * bs + 4]),   # unaligned 4
+            np.arange(9 * bs + 3, 9 * bs + 19) % (nb * bs),  # unaligned 16 (may cross a block)
+            np.array([-1, 11 * bs + 7, -1, 0]),              # padding and scattered
+            rng.permutation(np.arange(4 * bs, 5 * bs))[:7]]  # ragged tail of 7
+    slots = np.concatenate(runs).astype(np.int64)
+    assert len(np.unique(slots[slots >= 0])) == int((slots >= 0).sum())   # no slot twice
+    T = len(slots)
+    g = torch.Generator().manual_seed(bs * d)
+    k = (torch.randn(T, n_kv, d, generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn(T, n_kv, d, generator=g) * 3).to(torch.bfloat16)
+    kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    pa.pa_reshape_and_cache_quant(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(slots).cuda(),
+                                  k_scale=0.05, v_scale=0.03)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    kq = torch.from_numpy(oracle.quantize_fp8(k, 0.05))
+    vq = torch.from_numpy(oracle.quantize_fp8(v, 0.03))
+    pool0 = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8)
+    ek, _ = oracle.cache_write(pool0, pool0, kq, kq, slots, bs)
+    ev = oracle.cache_write_vt(torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8), vq, slots, bs)
+    assert np.array_equal(kc.view(torch.uint8).cpu().numpy().reshape(-1), ek)
+    assert np.array_equal(vc.view(torch.uint8).cpu().numpy().reshape(-1), ev)
+
+
 @pytest.mark.parametrize("bs,d", [(16, 128), (32, 64)])
 def test_fp8_cache_write_of_codes_bit_exact(bs, d):
     """Rows that already hold E4M3 codes, written through pa_reshape_and_cache
