@@ -134,12 +134,6 @@ __device__ __forceinline__ uint32_t q_pair(const QT* p)
 {
     return __ldg(reinterpret_cast<const unsigned int*>(p));   // q already in the MMA type
 }
-template <>
-__device__ __forceinline__ uint32_t q_pair<__nv_bfloat16, __half>(const __nv_bfloat16* p)
-{
-    const float2 f = Cvt<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const unsigned int*>(p)));
-    return Cvt<__half>::pack(f.x, f.y);
-}
 
 template <typename T, typename QT, int D, int BS, int NS, bool FP8, bool MQ, int RU = 8>
 __global__ void __launch_bounds__(kDecWarps * 32, decode_ctas_per_sm(FP8, D, RU))
@@ -301,37 +295,85 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // zero (RU 8) or rows g + 8 (RU 16, in qb)
     uint32_t qa[D / 16][2];
     uint32_t qb[R16 ? D / 16 : 1][2];
+    float row_l2 = scale_log2;   // softmax scale (log2 domain) of row g's scores
     auto load_q = [&](const Unit& x) {
+        if constexpr (FP8 && std::is_same<QT, __nv_bfloat16>::value) {
+            // bf16 q over an FP8 pool: the raw bf16 pairs of row g, made fp16
+            // operands by scale_q once the unit starts (so their latency
+            // overlaps the combine)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            if constexpr (R16) {
-                if (g + 8 < x.nh) {
-                    const int hh = (x.r0 + g + 8) / nq, qi = x.r0 + g + 8 - hh * nq;
+            for (int kk = 0; kk < D / 16; ++kk) {
+                if (g < x.nh) {
+                    const int hh = (x.r0 + g) / nq, qi = x.r0 + g - hh * nq;
                     const QT* row =
                         q + ((static_cast<int64_t>(x.s) * nq + qi) * n_q + x.h0 + hh) * D + kk * 16;
-                    qb[kk][0] = q_pair<QT, T>(row + 2 * t4);
-                    qb[kk][1] = q_pair<QT, T>(row + 2 * t4 + 8);
+                    qa[kk][0] = __ldg(reinterpret_cast<const unsigned int*>(row + 4 * t4));
+                    qa[kk][1] = __ldg(reinterpret_cast<const unsigned int*>(row + 4 * t4 + 2));
                 } else {
-                    qb[kk][0] = 0u;
-                    qb[kk][1] = 0u;
+                    qa[kk][0] = qa[kk][1] = 0u;
                 }
             }
-            if (g < x.nh) {
-                const int hh = (x.r0 + g) / nq, qi = x.r0 + g - hh * nq;
-                const QT* row =
-                    q + ((static_cast<int64_t>(x.s) * nq + qi) * n_q + x.h0 + hh) * D + kk * 16;
-                if constexpr (FP8) {
-                    // k order of the FP8 fragments: columns 4*t4 .. 4*t4+3 of the chunk
-                    qa[kk][0] = q_pair<QT, T>(row + 4 * t4);
-                    qa[kk][1] = q_pair<QT, T>(row + 4 * t4 + 2);
-                } else {
-                    qa[kk][0] = q_pair<QT, T>(row + 2 * t4);
-                    qa[kk][1] = q_pair<QT, T>(row + 2 * t4 + 8);
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                if constexpr (R16) {
+                    if (g + 8 < x.nh) {
+                        const int hh = (x.r0 + g + 8) / nq, qi = x.r0 + g + 8 - hh * nq;
+                        const QT* row =
+                            q + ((static_cast<int64_t>(x.s) * nq + qi) * n_q + x.h0 + hh) * D + kk * 16;
+                        qb[kk][0] = q_pair<QT, T>(row + 2 * t4);
+                        qb[kk][1] = q_pair<QT, T>(row + 2 * t4 + 8);
+                    } else {
+                        qb[kk][0] = 0u;
+                        qb[kk][1] = 0u;
+                    }
                 }
-            } else {
-                qa[kk][0] = 0u;
-                qa[kk][1] = 0u;
+                if (g < x.nh) {
+                    const int hh = (x.r0 + g) / nq, qi = x.r0 + g - hh * nq;
+                    const QT* row =
+                        q + ((static_cast<int64_t>(x.s) * nq + qi) * n_q + x.h0 + hh) * D + kk * 16;
+                    if constexpr (FP8) {
+                        // k order of the FP8 fragments: columns 4*t4 .. 4*t4+3 of the chunk
+                        qa[kk][0] = q_pair<QT, T>(row + 4 * t4);
+                        qa[kk][1] = q_pair<QT, T>(row + 4 * t4 + 2);
+                    } else {
+                        qa[kk][0] = q_pair<QT, T>(row + 2 * t4);
+                        qa[kk][1] = q_pair<QT, T>(row + 2 * t4 + 8);
+                    }
+                } else {
+                    qa[kk][0] = 0u;
+                    qa[kk][1] = 0u;
+                }
             }
+        }
+    };
+    // bf16 q over an FP8 pool -> fp16 operands (whole warp).  The quad's
+    // threads hold row g's columns 16*kk + 4*t4 .. +3; they meet on its largest
+    // magnitude (bf16 bits order as integers), the row is scaled by 2^-e so
+    // that this lands in [2^14, 2^15), exact for every element down to 2^-29 of
+    // the largest, and 2^e goes into the row's softmax scale: no bf16 query
+    // overflows fp16 or sinks into its subnormals.
+    auto scale_q = [&]() {
+        if constexpr (FP8 && std::is_same<QT, __nv_bfloat16>::value) {
+            uint32_t amax = 0;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    amax = max(amax, max(qa[kk][h] & 0x7FFFu, (qa[kk][h] >> 16) & 0x7FFFu));
+            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            // e from the exponent field (bf16 subnormals take the floor, -100)
+            const int e = amax == 0u ? 0 : max(static_cast<int>((amax >> 7) & 0xFFu) - 141, -100);
+            row_l2 = scale_log2 * __int_as_float((127 + e) << 23);    // exact: powers of two
+            const float down = __int_as_float((127 - e) << 23);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 f = Cvt<__nv_bfloat16>::unpack(qa[kk][h]);
+                    qa[kk][h] = Cvt<__half>::pack(f.x * down, f.y * down);
+                }
         }
     };
     // stage k of a unit (blk = its block ids, kvh_ its KV head) into this
@@ -406,6 +448,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 for (int k = 0; k < min(NS, my_n); ++k) issue(s_blk[cb], kvh, k, kt);
             }
 
+            scale_q();
 #pragma unroll
             for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             m_run = -INFINITY;
@@ -514,7 +557,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int p = pos0 + (FP8 ? 4 * t4 + 2 * nt + e : nt * 8 + 2 * t4 + e);
-                        const float z = p < lim ? sc[nt][e] * scale_log2 : -INFINITY;
+                        const float z = p < lim ? sc[nt][e] * row_l2 : -INFINITY;
                         sc[nt][e] = z;
                         mx = fmaxf(mx, z);
                     }

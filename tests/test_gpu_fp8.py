@@ -163,6 +163,28 @@ def test_fp8_decode_full_size_all_outputs():
     assert check_low_precision(out_lp, ref, wl.dtype) <= 0.0
 
 
+@pytest.mark.parametrize("q_pow2", [24, -30])
+@pytest.mark.parametrize("d", [128, 64])
+def test_fp8_decode_bf16_queries_outside_fp16_range(q_pow2, d):
+    """bf16 queries far above fp16's largest value or below its smallest normal
+    over an FP8 pool (the decode MMAs run on fp16 operands: each q row is
+    scaled by a power of two first, undone in the row's softmax scale).  q
+    times 2^k with the attention scale times 2^-k gives the same scores, so the
+    oracle's outputs for the unscaled q are the reference."""
+    wl = inputs.random_case(41, 4, 32, 8, d, 16, torch.bfloat16, [1, 40, 700, 2100],
+                            cache_dtype=torch.float8_e4m3fn, kv_scale=1.0 / 64)
+    st = PagedStep(wl, out_dtype=torch.float32)
+    st.step()
+    out = torch.full(tuple(st.out.shape), float("nan"), dtype=torch.float32, device="cuda")
+    q = st.q * 2.0 ** q_pow2                                  # exact: a power of two
+    pa.pa_decode(out, q, st.k_cache, st.v_cache, st.block_tables, st.context_lens,
+                 wl.scale * 2.0 ** -q_pow2, wl.block_size, st.workspace, **st.kv_scales)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert torch.isfinite(q.float()).all() and torch.equal(q.double() * 2.0 ** -q_pow2, st.q.double())
+    assert max_err(out, oracle_decode(st)) <= 2e-3
+
+
 def _fp8_prefill_case(seed, specs, n_q, n_kv, d, bs, act, scale, out_dtype=torch.float32,
                       v_scale=None, q_pow2=0):
     """specs: list of (cached tokens, chunk).  The context and the chunk go
