@@ -129,6 +129,17 @@ __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_
         : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
+// Plain (non-tensor) bulk copy of `bytes` contiguous bytes global -> shared,
+// completing on the mbarrier; both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 template <typename QT, typename T>
 __device__ __forceinline__ uint32_t q_pair(const QT* p)
 {
@@ -138,7 +149,7 @@ __device__ __forceinline__ uint32_t q_pair(const QT* p)
 template <typename T, typename QT, int D, int BS, int NS, bool FP8, bool MQ, int RU = 8>
 __global__ void __launch_bounds__(kDecWarps * 32, decode_ctas_per_sm(FP8, D, RU))
 decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
+                  const uint8_t* __restrict__ v_codes, void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
                   const int32_t* __restrict__ context_lens, int num_seqs, int n_q, int nq_arg,
                   int n_kv, int group, int num_blocks, float scale_log2, float v_scale,
@@ -389,7 +400,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
         if constexpr (FP8) {
             tma_load_2d(kdst, &kmap, 0, row, bar);                       // 16 rows x D codes
-            tma_load_2d(vdst, &vmap, (c % kCPB) * kRows, (b * n_kv + kvh_) * D, bar);  // D x 16
+            if constexpr (BS == kRows)   // the block's transposed slab: D x 16 contiguous codes
+                bulk_load(vdst, v_codes + (static_cast<int64_t>(b) * n_kv + kvh_) * D * BS,
+                          Cfg::kSlabBytes, bar);
+            else
+                tma_load_2d(vdst, &vmap, (c % kCPB) * kRows, (b * n_kv + kvh_) * D, bar);  // D x 16
         } else {
 #pragma unroll
             for (int hx = 0; hx < kHalves; ++hx) {
@@ -868,7 +883,7 @@ cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
     cfg.attrs = attr;
     cfg.numAttrs = ticket ? 0 : 1;
     return cudaLaunchKernelEx(
-        &cfg, kern, kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables,
+        &cfg, kern, kmap, vmap, static_cast<const uint8_t*>(a.v_cache), a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables,
         a.max_blocks, a.context_lens, a.num_seqs, a.n_q, a.q_per_seq, a.cache.n_kv_heads, group,
         a.cache.num_blocks, FP8 ? scale_log2 * a.cache.k_scale : scale_log2,
         FP8 ? a.cache.v_scale : 1.f, a.ws_ml, a.ws_acc, a.part_tokens, a.max_parts, ticket, a.err);
