@@ -69,9 +69,13 @@ typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
  * each stored code c means decode_e4m3(c) * k_scale for K (v_scale for V);
  * act_dtype (PA_BF16 or PA_F16) is the dtype of q and of the K/V rows given
  * to pa_reshape_and_cache_quant.  The three fields are ignored otherwise.
- * In FP8 pools the V codes of each (block, KV head) are stored transposed,
- * v_cache [num_blocks][n_kv_heads][head_dim][block_size], so that the decode
- * kernel reads pairs of tokens per head-dim element; K keeps the layout above. */
+ * In FP8 pools the V codes of each 16-token piece of a (block, KV head) are
+ * stored transposed, v_cache [num_blocks][n_kv_heads][block_size / 16]
+ * [head_dim][16]: the code of slot offset o, element i sits at
+ * [b][h][o / 16][i][o % 16].  A piece (head_dim x 16 codes) is contiguous, so
+ * the kernels fetch it with one bulk copy, and a 16-byte row holds the 16
+ * tokens of one head-dim element, the order the P.V fragments use; K keeps
+ * the layout above. */
 typedef struct {
     int num_blocks;
     int block_size;
@@ -227,9 +231,9 @@ pa_status pa_decode_no_alloc(void* out, pa_dtype out_dtype, const void* q,
  *                     written).
  *   workspace       : reserved; pass NULL / 0 (pa_prefill_workspace_size is 0).
  * bf16, fp16 and FP8 E4M3 pools (f32 pools return PA_ERR_UNSUPPORTED).  FP8
- * pools keep V transposed per block as for decode; their codes are widened
- * exactly to act_dtype on chip and the scales are folded into the softmax
- * scale (k_scale) and the output (v_scale). */
+ * pools keep V transposed per 16-token piece as for decode; their codes are
+ * widened exactly to fp16 on chip (every E4M3 value is an fp16 value) and the
+ * scales are folded into the softmax scale (k_scale) and the output (v_scale). */
 pa_status pa_prefill_chunk(void* out, pa_dtype out_dtype, const void* q,
                            const void* k_cache, const void* v_cache, const pa_cache_desc* cache,
                            const int32_t* block_tables, int max_blocks_per_seq,

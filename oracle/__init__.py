@@ -64,7 +64,7 @@ def _load():
                 "orc_slot_mapping": (None, [P, I, I, P, P, I, P]),
                 "orc_cache_write": (None, [P, P, P, P, P, I, I, I, I, I, I]),
                 "orc_gather": (None, [P, P, I, I, I, I, I, P]),
-                "orc_cache_write_vt": (None, [P, P, P, I, I, I, I, I, I]),
+                "orc_cache_write_vt": (None, [P, P, P, I, I, I, I, I, I, I]),
                 "orc_copy_blocks": (None, [P, P, P, P, P, I, L]),
                 "orc_fp8_e4m3_encode": (C.c_uint8, [C.c_float]),
                 "orc_fp8_e4m3_decode": (D, [C.c_uint8]),
@@ -202,14 +202,16 @@ def cache_write(k_cache, v_cache, k, v, slots, block_size: int):
 
 
 def cache_write_vt(v_cache, v, slots, block_size: int):
-    """Returns the new byte array of a V pool stored transposed per (block,
-    head), [NB][n_kv][d][bs], after writing rows of v [T][n_kv][d]."""
-    NB, n_kv, d, bs = v_cache.shape
-    assert bs == block_size
+    """Returns the new byte array of a V pool stored transposed per piece of
+    P tokens of each (block, head), [NB][n_kv][bs / P][d][P] (the shape of
+    v_cache gives P), after writing rows of v [T][n_kv][d]."""
+    NB, n_kv, n_pieces, d, piece = v_cache.shape
+    assert n_pieces * piece == block_size
     eb = v_cache.element_size()
     vc, vb = _bytes(v_cache), _bytes(v)
     slots = _c(slots, np.int64)
-    _load().orc_cache_write_vt(_ptr(vc), _ptr(vb), _ptr(slots), len(slots), NB, n_kv, bs, d, eb)
+    _load().orc_cache_write_vt(_ptr(vc), _ptr(vb), _ptr(slots), len(slots), NB, n_kv, block_size,
+                               d, eb, piece)
     return vc
 
 

@@ -159,8 +159,10 @@ void orc_cache_write(uint8_t* k_cache, uint8_t* v_cache, const uint8_t* k, const
 }
 
 void orc_cache_write_vt(uint8_t* v_cache, const uint8_t* v, const int64_t* slots, int T,
-                        int num_blocks, int n_kv, int block_size, int head_dim, int elem_bytes)
+                        int num_blocks, int n_kv, int block_size, int head_dim, int elem_bytes,
+                        int piece)
 {
+    const int pieces = block_size / piece;
     for (int t = 0; t < T; ++t) {
         int64_t slot = slots[t];
         if (slot < 0) continue;
@@ -168,8 +170,8 @@ void orc_cache_write_vt(uint8_t* v_cache, const uint8_t* v, const int64_t* slots
         if (b >= num_blocks) continue;
         for (int h = 0; h < n_kv; ++h)
             for (int i = 0; i < head_dim; ++i) {
-                size_t dst = ((((size_t)b * n_kv + h) * head_dim + (size_t)i) * block_size + (size_t)o) *
-                             elem_bytes;
+                size_t dst = (((((size_t)b * n_kv + h) * pieces + (size_t)(o / piece)) * head_dim +
+                               (size_t)i) * piece + (size_t)(o % piece)) * elem_bytes;
                 size_t src = (((size_t)t * n_kv + h) * head_dim + (size_t)i) * elem_bytes;
                 memcpy(v_cache + dst, v + src, (size_t)elem_bytes);
             }

@@ -77,11 +77,14 @@ void orc_cache_write(uint8_t* k_cache, uint8_t* v_cache, const uint8_t* k, const
                      const int64_t* slots, int T, int num_blocks, int n_kv, int block_size,
                      int head_dim, int elem_bytes);
 
-/* Same append for a V pool stored transposed per (block, head):
- * [num_blocks][n_kv][head_dim][block_size], i.e. element i of the row that
- * goes to slot (b, o) lands at [b][h][i][o]. */
+/* Same append for a V pool stored transposed per piece of `piece` tokens of
+ * a (block, head): [num_blocks][n_kv][block_size / piece][head_dim][piece],
+ * i.e. element i of the row that goes to slot (b, o) lands at
+ * [b][h][o / piece][i][o % piece].  piece divides block_size; piece =
+ * block_size is the whole block transposed. */
 void orc_cache_write_vt(uint8_t* v_cache, const uint8_t* v, const int64_t* slots, int T,
-                        int num_blocks, int n_kv, int block_size, int head_dim, int elem_bytes);
+                        int num_blocks, int n_kv, int block_size, int head_dim, int elem_bytes,
+                        int piece);
 
 /* [Sharing] copy-on-write / swap: for i < n, copy the whole physical block
  * map[i][0] of the source pools (all KV heads, all rows, K and V) over block

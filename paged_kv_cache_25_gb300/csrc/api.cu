@@ -290,8 +290,9 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
         return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
     unsigned* err = device_error_word();
     if (!err) return fail(PA_ERR_CUDA, "cannot locate the device error word");
-    // FP8 pools keep V transposed per block: the rows (codes already) go
-    // through the FP8 writer, which copies them and lays V out that way
+    // FP8 pools keep V transposed per 16-token piece of a block: the rows
+    // (codes already) go through the FP8 writer, which copies them and lays V
+    // out that way
     cudaError_t e = cache->dtype == PA_FP8_E4M3
                         ? launch_cache_write_fp8(k, v, PA_FP8_E4M3, k_cache, v_cache, slot_mapping,
                                                  num_tokens, *cache, err,

@@ -60,7 +60,8 @@ cudaError_t launch_cache_write(const void* k, const void* v, void* kc, void* vc,
 // Write into an FP8 E4M3 pool: 16 input elements of one (token, head) row
 // become 16 codes: code = e4m3_rn_satfinite(x / scale) with x / scale an IEEE
 // fp32 division (or, for rows given as codes, the codes themselves).  K keeps
-// the row layout; V codes go to the transposed V slab, [head_dim][block_size].
+// the row layout; V codes go to the transposed slab of their 16-token piece of
+// the block, [block_size / 16][head_dim][16].
 template <typename TI>
 __device__ __forceinline__ float load_as_float(const TI* p, int i);
 template <> __device__ __forceinline__ float load_as_float<float>(const float* p, int i) { return p[i]; }
@@ -108,9 +109,9 @@ __device__ __forceinline__ uint4 codes16<uint8_t>(const uint8_t* src, float)
 // 16 bytes per thread (a row's pieces are neighbours: coalesced).  V codes are
 // transposed through shared memory, [head][d][16 tokens], and then written one
 // (head, d) row of the slab per thread: 16 bytes when the 16 tokens fill 16
-// aligned consecutive slots (a chunk of a prompt), 4 bytes for each aligned
-// run of 4 consecutive slots, single bytes otherwise (one decode token per
-// sequence lands in 16 different blocks).
+// aligned consecutive slots (one whole 16-token piece: a chunk of a prompt),
+// 4 bytes for each aligned run of 4 consecutive slots, single bytes otherwise
+// (one decode token per sequence lands in 16 different blocks).
 constexpr int kFp8Tok = 16;
 
 template <typename TI, int D>
@@ -175,7 +176,7 @@ cache_write_fp8_kernel(const TI* __restrict__ k, const TI* __restrict__ v, uint8
     const uint8_t* row = vt[rh][d];
     auto dst = [&](int64_t sl) {   // byte address of slot sl's code in row d of head vh
         const int64_t b = sl / block_size, o = sl - b * block_size;
-        return vc + ((b * n_kv + vh) * D + d) * block_size + o;
+        return vc + (((b * n_kv + vh) * (block_size / 16) + o / 16) * D + d) * 16 + (o & 15);
     };
     if (s_run16) {
         *reinterpret_cast<uint4*>(dst(s_slot[0])) = *reinterpret_cast<const uint4*>(row);

@@ -95,7 +95,7 @@ constexpr int decode_stages()
 }
 
 // FP8 pools: a stage holds 16 rows of E4M3 K codes (swizzled rows of D bytes)
-// and the matching D x 16 tile of the transposed V codes.
+// and the matching D x 16 piece of the transposed V codes (as in the pool).
 // RU: rows of the MMA tile a work unit fills (8 = one sub-group of up to 8
 // heads with P's hi/lo halves in rows 0-7 / 8-15; 16 = sixteen (head, query)
 // rows, P's halves in two MMAs).
@@ -129,17 +129,6 @@ __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_
         : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
-// Plain (non-tensor) bulk copy of `bytes` contiguous bytes global -> shared,
-// completing on the mbarrier; both addresses 16-byte aligned, bytes a
-// multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 template <typename QT, typename T>
 __device__ __forceinline__ uint32_t q_pair(const QT* p)
 {
@@ -149,7 +138,8 @@ __device__ __forceinline__ uint32_t q_pair(const QT* p)
 template <typename T, typename QT, int D, int BS, int NS, bool FP8, bool MQ, int RU = 8>
 __global__ void __launch_bounds__(kDecWarps * 32, decode_ctas_per_sm(FP8, D, RU))
 decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  const uint8_t* __restrict__ v_codes, void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
+                  const uint8_t* __restrict__ v_codes, void* __restrict__ out, pa_dtype out_dtype,
+                  const QT* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
                   const int32_t* __restrict__ context_lens, int num_seqs, int n_q, int nq_arg,
                   int n_kv, int group, int num_blocks, float scale_log2, float v_scale,
@@ -233,7 +223,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     uint32_t kt = 0;   // stages this warp has consumed so far: its ring position and phase
     if (lane == 0) {
         prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
+        if constexpr (!FP8) prefetch_tensormap(&vmap);   // (FP8 V: bulk copies)
     }
 
     // Units are handed out dynamically: unit blockIdx.x first, then tickets
@@ -400,11 +390,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
         if constexpr (FP8) {
             tma_load_2d(kdst, &kmap, 0, row, bar);                       // 16 rows x D codes
-            if constexpr (BS == kRows)   // the block's transposed slab: D x 16 contiguous codes
-                bulk_load(vdst, v_codes + (static_cast<int64_t>(b) * n_kv + kvh_) * D * BS,
-                          Cfg::kSlabBytes, bar);
-            else
-                tma_load_2d(vdst, &vmap, (c % kCPB) * kRows, (b * n_kv + kvh_) * D, bar);  // D x 16
+            // the piece's transposed V codes: D x 16, contiguous in the pool
+            bulk_load(vdst, v_codes + ((static_cast<int64_t>(b) * n_kv + kvh_) * kCPB + c % kCPB) *
+                                          Cfg::kSlabBytes,
+                      Cfg::kSlabBytes, bar);
         } else {
 #pragma unroll
             for (int hx = 0; hx < kHalves; ++hx) {
@@ -841,15 +830,12 @@ cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
         if (per_sm < 1) per_sm = 1;
     });
     if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap{}, vmap{};
     const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
     if constexpr (FP8) {
-        // K: rows of D codes, 128- (D 128) or 64-byte (D 64) swizzle; V: the
-        // transposed slabs viewed as rows of block_size codes, one row per
-        // (block, head, head-dim element)
-        const uint64_t vrows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * D;
-        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, D, kRows, D) != PA_OK ||
-            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, BS, vrows, kRows, D, 0) != PA_OK)
+        // K: rows of D codes, 128- (D 128) or 64-byte (D 64) swizzle; V's
+        // 16-token pieces are plain bulk copies (the kernel leaves vmap unused)
+        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, D, kRows, D) != PA_OK)
             return cudaErrorInvalidValue;
     } else {
         if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, kRows) != PA_OK ||
@@ -883,10 +869,11 @@ cudaError_t run_mma(const DecodeArgs& a, cudaStream_t s, float scale_log2)
     cfg.attrs = attr;
     cfg.numAttrs = ticket ? 0 : 1;
     return cudaLaunchKernelEx(
-        &cfg, kern, kmap, vmap, static_cast<const uint8_t*>(a.v_cache), a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables,
-        a.max_blocks, a.context_lens, a.num_seqs, a.n_q, a.q_per_seq, a.cache.n_kv_heads, group,
-        a.cache.num_blocks, FP8 ? scale_log2 * a.cache.k_scale : scale_log2,
-        FP8 ? a.cache.v_scale : 1.f, a.ws_ml, a.ws_acc, a.part_tokens, a.max_parts, ticket, a.err);
+        &cfg, kern, kmap, vmap, static_cast<const uint8_t*>(a.v_cache), a.out, a.out_dtype,
+        static_cast<const QT*>(a.q), a.block_tables, a.max_blocks, a.context_lens, a.num_seqs,
+        a.n_q, a.q_per_seq, a.cache.n_kv_heads, group, a.cache.num_blocks,
+        FP8 ? scale_log2 * a.cache.k_scale : scale_log2, FP8 ? a.cache.v_scale : 1.f, a.ws_ml,
+        a.ws_acc, a.part_tokens, a.max_parts, ticket, a.err);
 }
 
 // Tensor-core kernels by shape; cudaErrorNotSupported for other shapes.

@@ -153,6 +153,7 @@ __device__ __forceinline__ uint4 keep_codes(uint4 c, int keep)
 template <typename T, typename QT, int D, int BS, bool F8 = false>
 __global__ void __launch_bounds__(PfWarps<F8>::kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const uint8_t* __restrict__ k_codes, const uint8_t* __restrict__ v_codes,
                   void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
                   const int32_t* __restrict__ block_tables, int max_blocks,
                   const int32_t* __restrict__ q_start, const int32_t* __restrict__ context_lens,
@@ -288,10 +289,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         set_error(err, PA_ERR_OUT_OF_RANGE);
                         b = 0;
                     }
-                    if (k_chunk)   // 16 rows of D codes
-                        tma_load_2d(buf + x * 16 * D, &kmap, 0, (b * n_kv + kvh) * BS + key0 % BS, bar);
-                    else           // D rows of 16 codes (the pool's transposed slab)
-                        tma_load_2d(buf + x * 16 * D, &vmap, key0 % BS, (b * n_kv + kvh) * D, bar);
+                    // 16 rows of D codes (K), or the D x 16 transposed piece
+                    // (V): 16 * D contiguous bytes of the pool either way
+                    const int64_t bh = static_cast<int64_t>(b) * n_kv + kvh;
+                    const uint8_t* src =
+                        k_chunk ? k_codes + (bh * BS + key0 % BS) * D
+                                : v_codes + (bh * (BS / 16) + (key0 % BS) / 16) * (16 * D);
+                    bulk_load(buf + x * 16 * D, src, 16 * D, bar);
                 }
             }
         };
@@ -301,10 +305,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             for (int m = n; m < min(n + 2, total); ++m)
                 mbar_wait(smem_u32(&cbars[m & 1]), (m >> 1) & 1, err);
         };
-        if (lane == 0) {
-            prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
-        }
         for (int n = 0; n < min(2, total); ++n) request(n);
 #pragma unroll 1
         for (int n = 0; n < total; ++n) {
@@ -777,16 +777,9 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
                                         static_cast<int>(Ly::kDynBytes));
     });
     if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap kmap, vmap;
-    const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
-    if constexpr (F8) {
-        // codes without swizzle: K boxes of 16 rows x D codes; V^T boxes of D
-        // rows x 16 codes of the transposed [d][block_size] slabs
-        const uint64_t vrows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * D;
-        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, D, 16, 0) != PA_OK ||
-            encode_pool_map(&vmap, a.v_cache, a.cache.dtype, BS, vrows, 16, D, 0) != PA_OK)
-            return cudaErrorInvalidValue;
-    } else {
+    CUtensorMap kmap{}, vmap{};
+    if constexpr (!F8) {   // (FP8 codes: plain bulk copies, the maps stay unused)
+        const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
         if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK ||
             encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK)
             return cudaErrorInvalidValue;
@@ -796,7 +789,8 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
                           (kTcTiles * kTcRows);
     dim3 grid(static_cast<unsigned>(tiles), a.cache.n_kv_heads, a.num_reqs);
     kern<<<grid, PfWarps<F8>::kThreads, Ly::kDynBytes, s>>>(
-        kmap, vmap, a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
+        kmap, vmap, static_cast<const uint8_t*>(a.k_cache), static_cast<const uint8_t*>(a.v_cache),
+        a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
         a.q_start, a.context_lens, a.max_q, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
         F8 ? sl2 * a.cache.k_scale : sl2, F8 ? a.cache.v_scale : 1.f, a.err);
     return cudaGetLastError();

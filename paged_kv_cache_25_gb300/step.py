@@ -90,8 +90,9 @@ class PagedStep:
         if self.fp8:
             self.k_cache = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8,
                                       device=dev).view(torch.float8_e4m3fn)
-            # FP8 V codes are stored transposed per (block, head): [d][block_size]
-            self.v_cache = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8,
+            # FP8 V codes are stored transposed per 16-token piece of a
+            # (block, head): [block_size / 16][d][16]
+            self.v_cache = torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8,
                                       device=dev).view(torch.float8_e4m3fn)
         else:
             self.k_cache = torch.full((nb, n_kv, bs, d), float("nan"), dtype=wl.dtype, device=dev)

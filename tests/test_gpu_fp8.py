@@ -37,7 +37,8 @@ def test_fp8_cache_write_whole_pool_bit_exact(act, scale):
     slots = np.random.default_rng(3).permutation(nb * bs)[:T].astype(np.int64)
     slots[5] = -1                                               # padding token
     kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
-    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8,
+                    device="cuda").view(torch.float8_e4m3fn)
     pa.pa_reshape_and_cache_quant(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(slots).cuda(),
                                   k_scale=scale, v_scale=scale)
     torch.cuda.synchronize()
@@ -46,8 +47,9 @@ def test_fp8_cache_write_whole_pool_bit_exact(act, scale):
     vq = torch.from_numpy(oracle.quantize_fp8(v, scale))
     pool0 = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8)
     ek, _ = oracle.cache_write(pool0, pool0, kq, vq, slots, bs)
-    # V codes land in the transposed layout [block][head][d][offset]
-    ev = oracle.cache_write_vt(torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8), vq, slots, bs)
+    # V codes land in the transposed layout [block][head][offset / 16][d][offset % 16]
+    ev = oracle.cache_write_vt(torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8),
+                               vq, slots, bs)
     assert np.array_equal(kc.view(torch.uint8).cpu().numpy().reshape(-1), ek)
     assert np.array_equal(vc.view(torch.uint8).cpu().numpy().reshape(-1), ev)
     # the negative-zero code is among the expected bytes of both pools (unless
@@ -78,7 +80,8 @@ def test_fp8_cache_write_slot_patterns_bit_exact(bs, d):
     k = (torch.randn(T, n_kv, d, generator=g) * 3).to(torch.bfloat16)
     v = (torch.randn(T, n_kv, d, generator=g) * 3).to(torch.bfloat16)
     kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
-    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8,
+                    device="cuda").view(torch.float8_e4m3fn)
     pa.pa_reshape_and_cache_quant(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(slots).cuda(),
                                   k_scale=0.05, v_scale=0.03)
     torch.cuda.synchronize()
@@ -87,7 +90,8 @@ def test_fp8_cache_write_slot_patterns_bit_exact(bs, d):
     vq = torch.from_numpy(oracle.quantize_fp8(v, 0.03))
     pool0 = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8)
     ek, _ = oracle.cache_write(pool0, pool0, kq, kq, slots, bs)
-    ev = oracle.cache_write_vt(torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8), vq, slots, bs)
+    ev = oracle.cache_write_vt(torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8),
+                               vq, slots, bs)
     assert np.array_equal(kc.view(torch.uint8).cpu().numpy().reshape(-1), ek)
     assert np.array_equal(vc.view(torch.uint8).cpu().numpy().reshape(-1), ev)
 
@@ -109,11 +113,12 @@ def test_fp8_cache_write_of_codes_bit_exact(bs, d):
     pool0 = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8)
     ek, _ = oracle.cache_write(pool0, pool0, torch.from_numpy(codes_k), torch.from_numpy(codes_k),
                                slots, bs)
-    ev = oracle.cache_write_vt(torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8),
+    ev = oracle.cache_write_vt(torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8),
                                torch.from_numpy(codes_v), slots, bs)
     for entry in ("plain", "quant"):
         kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
-        vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+        vc = torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8,
+                        device="cuda").view(torch.float8_e4m3fn)
         sl = torch.from_numpy(slots).cuda()
         if entry == "plain":
             pa.pa_reshape_and_cache(k, v, kc, vc, sl, k_scale=0.5, v_scale=0.25)
@@ -205,7 +210,8 @@ def _fp8_prefill_case(seed, specs, n_q, n_kv, d, bs, act, scale, out_dtype=torch
     qs = [(torch.randn(n, n_q, d, generator=g) * 2.0 ** q_pow2).to(act) for _, n in specs]
     att = float(np.float32(2.0 ** -q_pow2 / np.sqrt(d)))
     kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
-    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8,
+                    device="cuda").view(torch.float8_e4m3fn)
     seq = np.concatenate([np.full(L, r, np.int32) for r, L in enumerate(lens)])
     pos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens])
     slots = torch.from_numpy(pa.pa_slot_mapping(tables, bs, seq, pos)).cuda()
@@ -296,7 +302,8 @@ def test_fp8_prefill_widens_every_code_exactly(act, subnormal):
     nb = -(-L // bs) + 2
     tables = np.arange(-(-L // bs), dtype=np.int32)[None, :]
     kc = torch.full((nb, n_kv, bs, d), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
-    vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    vc = torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8,
+                    device="cuda").view(torch.float8_e4m3fn)
     slots = torch.from_numpy(pa.pa_slot_mapping(tables, bs, np.zeros(L, np.int32),
                                                 np.arange(L, dtype=np.int32))).cuda()
     pa.pa_reshape_and_cache_quant(k.cuda(), vt.cuda(), kc, vc, slots, k_scale=1.0, v_scale=1.0)

@@ -38,7 +38,7 @@ class Case:
         shape = (nb, n_kv, bs, d)
         if pool_dt == torch.float8_e4m3fn:
             self.kc = torch.full(shape, 0x7F, dtype=torch.uint8, device="cuda").view(pool_dt)
-            self.vc = torch.full((nb, n_kv, d, bs), 0x7F, dtype=torch.uint8,
+            self.vc = torch.full((nb, n_kv, bs // 16, d, 16), 0x7F, dtype=torch.uint8,
                                  device="cuda").view(pool_dt)
             self.scales = {"k_scale": kv_scale, "v_scale": kv_scale}
         else:

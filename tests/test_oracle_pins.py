@@ -475,17 +475,22 @@ def test_fp8_quantize_divides_in_fp32_then_rounds():
     assert oracle.quantize_fp8(torch.tensor([9.0]), scale)[0] == 0x7E   # 720 saturates to 448
 
 
-def test_cache_write_transposed_v_layout():
-    """Row t of V that goes to slot (block b, offset o) lands column-wise:
-    element i at [b][h][i][o]; it holds the same values as the row-major pool."""
+@pytest.mark.parametrize("piece", [2, 4])
+def test_cache_write_transposed_v_layout(piece):
+    """Row t of V that goes to slot (block b, offset o) lands column-wise in
+    its piece of P tokens: element i at [b][h][o / P][i][o % P]; it holds the
+    same values as the row-major pool.  P = the block size is the whole block
+    transposed."""
     nb, n_kv, bs, d = 3, 2, 4, 5
-    v = torch.arange(2 * n_kv * d, dtype=torch.float32).reshape(2, n_kv, d) + 1
-    slots = [1 * bs + 2, 2 * bs + 0]
-    vt = oracle.cache_write_vt(torch.zeros(nb, n_kv, d, bs), v, slots, bs)
-    vt = torch.from_numpy(vt).view(torch.float32).reshape(nb, n_kv, d, bs)
-    assert torch.equal(vt[1, :, :, 2], v[0]) and torch.equal(vt[2, :, :, 0], v[1])
+    v = torch.arange(3 * n_kv * d, dtype=torch.float32).reshape(3, n_kv, d) + 1
+    slots = [1 * bs + 2, 2 * bs + 0, 0 * bs + 3]
+    vt = oracle.cache_write_vt(torch.zeros(nb, n_kv, bs // piece, d, piece), v, slots, bs)
+    vt = torch.from_numpy(vt).view(torch.float32).reshape(nb, n_kv, bs // piece, d, piece)
+    for t, s in enumerate(slots):
+        b, o = divmod(s, bs)
+        assert torch.equal(vt[b, :, o // piece, :, o % piece], v[t])
     assert int((vt != 0).sum()) == v.numel()
     _, vr = oracle.cache_write(torch.zeros(nb, n_kv, bs, d), torch.zeros(nb, n_kv, bs, d), v, v,
                                slots, bs)
-    vr = torch.from_numpy(vr).view(torch.float32).reshape(nb, n_kv, bs, d)
-    assert torch.equal(vr.transpose(2, 3), vt)
+    vr = torch.from_numpy(vr).view(torch.float32).reshape(nb, n_kv, bs // piece, piece, d)
+    assert torch.equal(vr.transpose(3, 4), vt)
