@@ -42,10 +42,10 @@ FALLBACK_HBM_GBS = 6800.0
 # K/V bytes of the captured launch, what was captured); a record of another
 # batch of the same workload is scaled by its unique K/V bytes.
 NCU_TRAFFIC = {
-    ("llama3-8b-bf16", "222c6a85c05167fc"): (2371994368 + 13491712, 2359717888,
+    ("llama3-8b-bf16", "8c018e5e71f5b98c"): (2372009472 + 13484800, 2359717888,
                                              "full 256-sequence batch, one-pass capture"),
-    ("llama3-8b-fp8", "222c6a85c05167fc"): (311070720 + 4660736, 308879360,
-                                            "64-sequence batch (--set full), scaled by unique K/V bytes"),
+    ("llama3-8b-fp8", "8c018e5e71f5b98c"): (1188431360 + 14343936, 1179858944,
+                                            "full 256-sequence batch, one-pass capture"),
 }
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
 # chunks as the 60 GB pool): bytes per launch
