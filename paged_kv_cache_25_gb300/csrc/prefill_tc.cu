@@ -24,13 +24,14 @@
 //             TMEM, applies the causal mask on absolute positions,
 //             runs the online softmax in base 2 with lazy rescaling (O in TMEM
 //             is rescaled only when the running max grows by more than 2^8),
-//             and writes P back over its scores in TMEM as hi + lo bf16/fp16
-//             halves (P V keeps ~16 bits of P); the P V MMA takes P straight
+//             and writes P back over its scores in TMEM: as hi + lo bf16
+//             halves with bf16 operands (P V keeps ~16 bits of P), as one fp16
+//             part with fp16 operands (11 bits); the P V MMA takes P straight
 //             from TMEM.  At the end O / l goes to global memory.
-// FP8 (E4M3) pools: three converter warps replace the two producers; they TMA
+// FP8 (E4M3) pools: three converter warps replace the two producers; they copy
 // the codes chunk by chunk into staging buffers and widen them exactly to fp16
-// in the same rings (V kept in the pool's transposed [d][keys] order, a K-major
-// operand of P V); keys at or past the context are written as zeros.  The
+// in the same rings (V kept in the pool's transposed [d][keys] pieces, a
+// K-major operand of P V); keys at or past the context are written as zeros.  The
 // MMAs run on fp16 operands (bf16 queries are scaled into fp16 per row).
 // k_scale is folded into the softmax scale and v_scale into the output.
 // All waits are bounded; the kernel never traps.
@@ -82,7 +83,8 @@ struct PfLayout {
     static constexpr uint32_t kOffCS = kOffV + kTcStages * kKBytes;  // FP8: 2 code buffers per converter
     static constexpr uint32_t kDynBytes = kOffCS + (F8 ? kF8Converters * 2 * kCodeBytes : 0) + 1024;
     // S_t at t * 128; P_t overwrites it, keys 32c .. 32c+31 as hi in columns
-    // 32c .. 32c+15 and lo in 32c+16 .. 32c+31 (two 16-bit values per column)
+    // 32c .. 32c+15 and (bf16 operands) lo in 32c+16 .. 32c+31 (two 16-bit
+    // values per column)
     static constexpr uint32_t kTmemS = 0;
     static constexpr uint32_t kTmemO = 256;                       // + t * D
     static_assert(kDynBytes <= 232448, "shared memory per CTA");
@@ -163,6 +165,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     using Ly = PfLayout<T, D, F8>;
     constexpr int kMmaWarp = PfWarps<F8>::kMma;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    // P for P V: fp16 operands (fp16 and FP8 pools) take P as one fp16 part,
+    // 11 significant bits, so each output moves by at most 2^-12 of the
+    // largest |v| it averages; bf16 operands take P as hi + lo bf16 parts
+    // (8 significant bits each, ~16 together)
+    constexpr bool kOneP = !kBf16;
     constexpr uint32_t kIdescQK = idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
     // P V: V as [keys][d] (MN-major) from 16-bit pools, as [d][keys] (K-major) from FP8
     constexpr uint32_t kIdescPV = idesc_f16(kBf16, false, !F8, kTcRows, D);
@@ -462,7 +469,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
                 umma_commit_elect(smem_u32(&s_full[t]));
             };
-            // O_t += P_t(j) V_j, P from TMEM (hi and lo halves of each 16 keys)
+            // O_t += P_t(j) V_j, P from TMEM (hi, and lo for bf16, of each 16 keys)
             auto issue_pv = [&](int t, int j) {
                 const int st = j % kTcStages;
                 const uint64_t dvs = dv + st * kKStage;
@@ -478,7 +485,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     const uint32_t vst = F8 ? (ks >> 2) * ((D * 128) >> 4) + (ks & 3) * 2
                                             : ks * (2048 >> 4);
                     umma_f16_ts_elect(d_o, a_p + col, dvs + vst, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-                    umma_f16_ts_elect(d_o, a_p + col + 16, dvs + vst, kIdescPV, 1u);
+                    if constexpr (!kOneP)   // bf16 operands: P's lo part too
+                        umma_f16_ts_elect(d_o, a_p + col + 16, dvs + vst, kIdescPV, 1u);
                 }
                 umma_commit_elect(smem_u32(&pv_done[t]));
             };
@@ -670,9 +678,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
             }
 
-            // pass 2, per 32 keys: exponent, row sum, hi/lo split, written over
-            // those 32 keys' own score columns (hi in the first 16, lo in the
-            // next 16), so no score is overwritten before it is read
+            // pass 2, per 32 keys: exponent, row sum, P (hi/lo split for bf16),
+            // written over those 32 keys' own score columns (hi in the first
+            // 16, lo in the next 16), so no score is overwritten before it is read
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -686,7 +694,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
                         const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
                         s4[i & 3] += p0 + p1;
-                        split_trunc<T>(p0, p1, ph[i], pl[i]);
+                        if constexpr (kOneP) ph[i] = Cvt<__half>::pack(p0, p1);
+                        else split_trunc<T>(p0, p1, ph[i], pl[i]);
                     }
                 } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
 #pragma unroll
@@ -695,11 +704,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         const float p0 = k <= p_abs ? fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc)) : 0.f;
                         const float p1 = k + 1 <= p_abs ? fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc)) : 0.f;
                         s4[i & 3] += p0 + p1;
-                        split_trunc<T>(p0, p1, ph[i], pl[i]);
+                        if constexpr (kOneP) ph[i] = Cvt<__half>::pack(p0, p1);
+                        else split_trunc<T>(p0, p1, ph[i], pl[i]);
                     }
                 }
-                tmem_st16(lane_addr + s_col + h2 * 32, ph);        // over the scores
-                tmem_st16(lane_addr + s_col + h2 * 32 + 16, pl);   // just read
+                tmem_st16(lane_addr + s_col + h2 * 32, ph);            // over the scores
+                if constexpr (!kOneP) tmem_st16(lane_addr + s_col + h2 * 32 + 16, pl);   // just read
 
             }
             l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
