@@ -50,8 +50,8 @@ NCU_TRAFFIC = {
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
 # chunks as the 60 GB pool): bytes per launch
 NCU_PREFILL_TRAFFIC = {
-    ("mixed-llama3-8b-bf16", "ac86ec92b3feb147"): (98359552 + 5173248, "compact pool, --set full"),
-    ("mixed-llama3-8b-fp8", "ac86ec92b3feb147"): (57597184 + 1532160, "compact pool, --set full"),
+    ("mixed-llama3-8b-bf16", "2d38b48613ecaf60"): (98304256 + 4817664, "compact pool, --set full"),
+    ("mixed-llama3-8b-fp8", "2d38b48613ecaf60"): (57562368 + 1563136, "compact pool, --set full"),
 }
 
 
