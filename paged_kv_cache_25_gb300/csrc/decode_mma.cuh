@@ -64,7 +64,7 @@ __device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dt
 // count of those variants fits 3 CTAs of 4 warps).
 constexpr int decode_ctas_per_sm(bool fp8, int D = 128, int RU = 8)
 {
-    return fp8 || (D == 64 && RU == 8) ? 3 : 2;
+    return RU == 4 ? 4 : (fp8 || (D == 64 && RU == 8) ? 3 : 2);
 }
 constexpr int kSmemPerSm = 233472;    // 228 KB of shared memory per SM
 // bound on the kernel's static shared memory (ptxas: 9,296 B at d 128 with a
@@ -98,7 +98,8 @@ constexpr int decode_stages()
 // and the matching D x 16 piece of the transposed V codes (as in the pool).
 // RU: rows of the MMA tile a work unit fills (8 = one sub-group of up to 8
 // heads with P's hi/lo halves in rows 0-7 / 8-15; 16 = sixteen (head, query)
-// rows, P's halves in two MMAs).
+// rows, P's halves in two MMAs; 4 = FP8 decode of up to 4 heads a KV head,
+// computed transposed: the 16 tokens of a stage are the MMA rows, see below).
 template <typename T, int D, int NS, bool FP8 = false, int RU = 8>
 struct DecodeCfg {
     static constexpr int kElem = FP8 ? 1 : static_cast<int>(sizeof(T));
@@ -149,7 +150,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     using Cfg = DecodeCfg<T, D, NS, FP8, RU>;
     static_assert(!FP8 || std::is_same<T, __half>::value, "FP8 pools compute in fp16");
     constexpr bool R16 = RU == 16;
-    static_assert(RU == 8 || (RU == 16 && MQ && !FP8), "16-row units: multi-query, 16-bit pools");
+    static_assert(RU == 8 || (RU == 16 && MQ && !FP8) || (RU == 4 && FP8 && !MQ),
+                  "16-row units: multi-query, 16-bit pools; 4-row units: FP8 decode");
+    // Transposed FP8 decode (RU 4): S^T = K q^T with the stage's 16 tokens as
+    // the M rows and 8 columns: the unit's <= 4 heads, then the same heads
+    // again (same q).  Columns 0-3 carry P's hi part and columns 4-7 its lo
+    // part, so O^T = V^T P^T (D rows, the V piece as it is stored) keeps ~22
+    // bits of P in one MMA per 16 rows of d.  Per stage: 8 + 8 MMAs instead of
+    // 16 + 16, and half the O accumulators.
+    constexpr bool kTr = RU == 4;
     constexpr int kHalves = D / 64;           // 64-column halves (one 128-byte swizzled row each)
     constexpr int kHalfTile = kRows * 128;
     constexpr int kCPB = BS / kRows;          // stages per block
@@ -297,6 +306,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     uint32_t qa[D / 16][2];
     uint32_t qb[R16 ? D / 16 : 1][2];
     float row_l2 = scale_log2;   // softmax scale (log2 domain) of row g's scores
+    // the unit row this thread's q fragments hold: row g, or (kTr) column g,
+    // whose head is g mod 4
+    const int gq = kTr ? (g & 3) : g;
     auto load_q = [&](const Unit& x) {
         if constexpr (FP8 && std::is_same<QT, __nv_bfloat16>::value) {
             // bf16 q over an FP8 pool: the raw bf16 pairs of row g, made fp16
@@ -304,8 +316,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             // overlaps the combine)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                if (g < x.nh) {
-                    const int hh = (x.r0 + g) / nq, qi = x.r0 + g - hh * nq;
+                if (gq < x.nh) {
+                    const int hh = (x.r0 + gq) / nq, qi = x.r0 + gq - hh * nq;
                     const QT* row =
                         q + ((static_cast<int64_t>(x.s) * nq + qi) * n_q + x.h0 + hh) * D + kk * 16;
                     qa[kk][0] = __ldg(reinterpret_cast<const unsigned int*>(row + 4 * t4));
@@ -329,8 +341,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         qb[kk][1] = 0u;
                     }
                 }
-                if (g < x.nh) {
-                    const int hh = (x.r0 + g) / nq, qi = x.r0 + g - hh * nq;
+                if (gq < x.nh) {
+                    const int hh = (x.r0 + gq) / nq, qi = x.r0 + gq - hh * nq;
                     const QT* row =
                         q + ((static_cast<int64_t>(x.s) * nq + qi) * n_q + x.h0 + hh) * D + kk * 16;
                     if constexpr (FP8) {
@@ -410,6 +422,24 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     float* red_m = red_o + kDecWarps * RU * D;                          // [warps][RU]
     float* red_l = red_m + kDecWarps * RU;                              // [warps][RU]
 
+    // FP8: tokens past the sequence may hold anything (even NaN): zero their
+    // codes in every row of the stage's transposed V piece (whole warp)
+    auto zero_v_tail = [&](uint32_t vbase, int valid) {
+        uint8_t* vt = smem + (vbase - smem_u32(smem));
+        for (int row = lane; row < D; row += 32) {
+            uint4 w = *reinterpret_cast<uint4*>(vt + row * 16);
+            uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int keep = min(4, max(0, valid - 4 * e));     // bytes kept
+                ww[e] &= keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+            }
+            *reinterpret_cast<uint4*>(vt + row * 16) = w;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    };
+
     // ---- the first unit: ids checked before any load is issued
     int64_t u = blockIdx.x;
     if (u >= units) return;                           // uniform over the CTA
@@ -429,9 +459,56 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     int cb = 0;                                       // s_blk buffer of the current unit
     bool issued = false;                              // its first stages are in flight
 
-    float o[D / 8][4];
-    float m_run, l_run;     // row g
-    float m_run1, l_run1;   // row g + 8 (RU 16)
+    // O accumulators: [D / 8] n-tiles of O (rows = heads), or (kTr) [D / 16]
+    // m-tiles of O^T (rows = d, columns = the 8 columns above)
+    constexpr int kOT = kTr ? D / 16 : D / 8;
+    float o[kOT][4];
+    float m_run, l_run;     // row g (kTr: column 2*t4)
+    float m_run1, l_run1;   // row g + 8 (RU 16; kTr: column 2*t4 + 1)
+    // this warp's partial rows (running max, sum, unnormalised O) -> the
+    // combine buffer [warp][row]
+    auto write_partials = [&]() {
+        if constexpr (kTr) {
+            if (t4 < 2) {   // columns 2*t4 and 2*t4 + 1: heads, hi and lo parts merged
+                float* dst = red_o + (warp * RU + 2 * t4) * D + g;
+#pragma unroll
+                for (int mt = 0; mt < kOT; ++mt) {
+                    dst[16 * mt] = o[mt][0];
+                    dst[16 * mt + 8] = o[mt][2];
+                    dst[D + 16 * mt] = o[mt][1];
+                    dst[D + 16 * mt + 8] = o[mt][3];
+                }
+                if (g == 0) {
+                    red_m[warp * RU + 2 * t4] = m_run;
+                    red_l[warp * RU + 2 * t4] = l_run;
+                    red_m[warp * RU + 2 * t4 + 1] = m_run1;
+                    red_l[warp * RU + 2 * t4 + 1] = l_run1;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                float* dst = red_o + (warp * RU + g) * D + nt * 8 + 2 * t4;
+                if constexpr (R16) {
+                    dst[0] = o[nt][0];
+                    dst[1] = o[nt][1];
+                    dst[8 * D] = o[nt][2];           // row g + 8
+                    dst[8 * D + 1] = o[nt][3];
+                } else {
+                    dst[0] = o[nt][0] + o[nt][2];
+                    dst[1] = o[nt][1] + o[nt][3];
+                }
+            }
+            if (t4 == 0) {
+                red_m[warp * RU + g] = m_run;
+                red_l[warp * RU + g] = l_run;
+                if constexpr (R16) {
+                    red_m[warp * RU + g + 8] = m_run1;
+                    red_l[warp * RU + g + 8] = l_run1;
+                }
+            }
+        }
+    };
     while (u < units) {
         const Unit nx = describe(un);
         // the next unit's block ids: in flight while this unit streams
@@ -453,8 +530,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
 
             scale_q();
+            // kTr: softmax scale of this thread's two columns (heads 2*t4 and
+            // 2*t4 + 1, mod 4), held by the quads g = 2*t4 and 2*t4 + 1
+            float cl2_0 = row_l2, cl2_1 = row_l2;
+            if constexpr (kTr) {
+                cl2_0 = __shfl_sync(0xffffffffu, row_l2, 8 * t4);
+                cl2_1 = __shfl_sync(0xffffffffu, row_l2, 8 * t4 + 4);
+            }
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            for (int i = 0; i < kOT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             m_run = -INFINITY;
             m_run1 = -INFINITY;
             l_run1 = 0.f;
@@ -471,197 +555,260 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const int valid = min(kRows, L - pos0);
                 const uint32_t kbase = ring + st * Cfg::kStageBytes;
                 const uint32_t vbase = kbase + Cfg::kSlabBytes;
-                float sc[2][4];
-                float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-
-                if constexpr (FP8) {
-                    if (valid < kRows) {
-                        // tokens past the sequence may hold anything (even NaN): zero
-                        // their codes in every row of the transposed V tile
-                        uint8_t* vt = smem + (vbase - smem_u32(smem));
-                        for (int row = lane; row < D; row += 32) {
-                            uint4 w = *reinterpret_cast<uint4*>(vt + row * 16);
-                            uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
+                if constexpr (kTr) {
+                    if (valid < kRows) zero_v_tail(vbase, valid);
+                    // S^T = K q^T.  Row r of the tile is token 4*((r&7)>>1) + 2*(r>>3)
+                    // + (r&1) of the stage: after the transpose below, P^T comes out
+                    // in the token order of the V fragments.  Fragment words hold four
+                    // consecutive codes (k order permuted as q was loaded).
+                    float st[4] = {0.f, 0.f, 0.f, 0.f}, st2[4] = {0.f, 0.f, 0.f, 0.f};
+                    {
+                        const int mi = lane >> 3, i = lane & 7;
+                        const int tok = 4 * (i >> 1) + 2 * (mi & 1) + (i & 1);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int keep = min(4, max(0, valid - 4 * e));     // bytes kept
-                                ww[e] &= keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
-                            }
-                            *reinterpret_cast<uint4*>(vt + row * 16) = w;
+                        for (int c2 = 0; c2 < D / 32; ++c2) {   // chunks 2*c2 and 2*c2 + 1
+                            const int cidx = 2 * c2 + (mi >> 1);
+                            const int sw = D == 128 ? (cidx ^ (tok & 7)) : (cidx ^ ((tok >> 1) & 3));
+                            uint32_t w[4], a[4];
+                            ldsm_x4(kbase + tok * D + (sw << 4), w[0], w[1], w[2], w[3]);
+                            e4m3x4_to_h2x2(w[0], a[0], a[2]);
+                            e4m3x4_to_h2x2(w[1], a[1], a[3]);
+                            MmaOp<T>::run(st, a, qa[2 * c2][0], qa[2 * c2][1]);
+                            e4m3x4_to_h2x2(w[2], a[0], a[2]);
+                            e4m3x4_to_h2x2(w[3], a[1], a[3]);
+                            MmaOp<T>::run(st2, a, qa[2 * c2 + 1][0], qa[2 * c2 + 1][1]);
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
                     }
-                    // S = Q K^T.  Column j of n-tile nt is token 4*(j/2) + 2*nt + j%2,
-                    // which leaves P in the token order the V fragments use below.
+                    // online softmax down the columns (log2 domain): this thread has
+                    // tokens tA and tA + 2 of columns 2*t4 and 2*t4 + 1; the column
+                    // max meets over the eight lanes of each t4
+                    const int tA = pos0 + 4 * (g >> 1) + (g & 1);
+                    const float z0 = tA < L ? (st[0] + st2[0]) * cl2_0 : -INFINITY;
+                    const float z1 = tA < L ? (st[1] + st2[1]) * cl2_1 : -INFINITY;
+                    const float z2 = tA + 2 < L ? (st[2] + st2[2]) * cl2_0 : -INFINITY;
+                    const float z3 = tA + 2 < L ? (st[3] + st2[3]) * cl2_1 : -INFINITY;
+                    float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-                        const int i = lane & 7;
-                        const int r = 4 * (i >> 1) + 2 * nt + (i & 1);
+                    for (int w = 4; w < 32; w <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, w));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, w));
+                    }
+                    // (every stage holds a visible token, so the maxima are finite)
+                    const float mn0 = fmaxf(m_run, mx0), mn1 = fmaxf(m_run1, mx1);
+                    if (__any_sync(0xffffffffu, mn0 != m_run || mn1 != m_run1)) {
+                        const float a0 = fast_exp2(m_run - mn0), a1 = fast_exp2(m_run1 - mn1);
+                        l_run *= a0;
+                        l_run1 *= a1;
 #pragma unroll
-                        for (int kq = 0; kq < D / 64; ++kq) {
-                            const int cidx = kq * 4 + (lane >> 3);
-                            const int sw = D == 128 ? (cidx ^ (r & 7)) : (cidx ^ ((r >> 1) & 3));
-                            uint32_t w[4];
-                            ldsm_x4(kbase + r * D + (sw << 4), w[0], w[1], w[2], w[3]);
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) {
-                                const int kk = kq * 4 + jj;
-                                const uint32_t a[4] = {qa[kk][0], 0u, qa[kk][1], 0u};
-                                uint32_t b0, b1;
-                                e4m3x4_to_h2x2(w[jj], b0, b1);
-                                // two accumulator chains (even / odd 16 columns) halve the
-                                // dependent MMA sequence per n-tile
-                                MmaOp<T>::run((jj & 1) ? sc2[nt] : sc[nt], a, b0, b1);
-                            }
+                        for (int mt = 0; mt < kOT; ++mt) {
+                            o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
                         }
-                        sc[nt][0] += sc2[nt][0]; sc[nt][1] += sc2[nt][1];
-                        sc[nt][2] += sc2[nt][2]; sc[nt][3] += sc2[nt][3];
+                    }
+                    m_run = mn0;
+                    m_run1 = mn1;
+                    const float p0 = fast_exp2(z0 - mn0), p1 = fast_exp2(z1 - mn1);
+                    const float p2 = fast_exp2(z2 - mn0), p3 = fast_exp2(z3 - mn1);
+                    l_run += p0 + p2;
+                    l_run1 += p1 + p3;
+                    // P^T as the B operand: columns 0-3 take P's hi part, columns 4-7
+                    // (the same heads) its lo part; each 8 x 8 block of the score
+                    // layout is transposed in registers
+                    uint32_t hu, lu, hv, lv;
+                    split_pair<T>(p0, p1, hu, lu);   // rows g: tokens tA
+                    split_pair<T>(p2, p3, hv, lv);   // rows g + 8: tokens tA + 2
+                    const uint32_t pb0 = movmatrix_trans(t4 < 2 ? hu : lu);
+                    const uint32_t pb1 = movmatrix_trans(t4 < 2 ? hv : lv);
+                    // O^T += V^T P^T: m-tile mt is rows 16*mt .. +15 of the V piece
+                    // (row d holds the stage's 16 tokens of element d)
+#pragma unroll
+                    for (int q2 = 0; q2 < D / 32; ++q2) {
+                        const int d_row = 32 * q2 + 8 * (lane >> 3) + (lane & 7);
+                        uint32_t w[4], a[4];
+                        ldsm_x4(vbase + d_row * 16, w[0], w[1], w[2], w[3]);
+                        e4m3x4_to_h2x2(w[0], a[0], a[2]);
+                        e4m3x4_to_h2x2(w[1], a[1], a[3]);
+                        MmaOp<T>::run(o[2 * q2], a, pb0, pb1);
+                        e4m3x4_to_h2x2(w[2], a[0], a[2]);
+                        e4m3x4_to_h2x2(w[3], a[1], a[3]);
+                        MmaOp<T>::run(o[2 * q2 + 1], a, pb0, pb1);
                     }
                 } else {
-                    if (valid < kRows) {
-                        // rows past the sequence may hold anything (even NaN): zero them in
-                        // V so that 0 * row stays 0 inside the MMA
-                        uint8_t* vgen = smem + (vbase - smem_u32(smem));
-                        const int nbytes = (kRows - valid) * 128;
-                        for (int hx = 0; hx < kHalves; ++hx)
-                            for (int off = lane * 16; off < nbytes; off += 32 * 16)
-                                *reinterpret_cast<uint4*>(vgen + hx * kHalfTile + valid * 128 + off) =
-                                    make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    // S = Q K^T for the 16 rows
+                    float sc[2][4];
+                    float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+
+                    if constexpr (FP8) {
+                        if (valid < kRows) zero_v_tail(vbase, valid);
+                        // S = Q K^T.  Column j of n-tile nt is token 4*(j/2) + 2*nt + j%2,
+                        // which leaves P in the token order the V fragments use below.
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                        for (int nt = 0; nt < 2; ++nt) {
+                            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                            const int i = lane & 7;
+                            const int r = 4 * (i >> 1) + 2 * nt + (i & 1);
 #pragma unroll
-                        for (int kc = 0; kc < D / 16; kc += 2) {
-                            const int r = nt * 8 + (lane & 7);
-                            const int chunk = kc * 2 + (lane >> 3);
-                            const uint32_t addr = kbase + (chunk >> 3) * kHalfTile + r * 128 +
-                                                  (((chunk & 7) ^ (r & 7)) << 4);
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4(addr, b0, b1, b2, b3);
-                            const uint32_t a0[4] = {qa[kc][0], R16 ? qb[R16 ? kc : 0][0] : 0u, qa[kc][1],
-                                                    R16 ? qb[R16 ? kc : 0][1] : 0u};
-                            const uint32_t a1[4] = {qa[kc + 1][0], R16 ? qb[R16 ? kc + 1 : 0][0] : 0u,
-                                                    qa[kc + 1][1], R16 ? qb[R16 ? kc + 1 : 0][1] : 0u};
-                            MmaOp<T>::run(sc[nt], a0, b0, b1);
-                            MmaOp<T>::run(sc[nt], a1, b2, b3);
+                            for (int kq = 0; kq < D / 64; ++kq) {
+                                const int cidx = kq * 4 + (lane >> 3);
+                                const int sw = D == 128 ? (cidx ^ (r & 7)) : (cidx ^ ((r >> 1) & 3));
+                                uint32_t w[4];
+                                ldsm_x4(kbase + r * D + (sw << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                                for (int jj = 0; jj < 4; ++jj) {
+                                    const int kk = kq * 4 + jj;
+                                    const uint32_t a[4] = {qa[kk][0], 0u, qa[kk][1], 0u};
+                                    uint32_t b0, b1;
+                                    e4m3x4_to_h2x2(w[jj], b0, b1);
+                                    // two accumulator chains (even / odd 16 columns) halve the
+                                    // dependent MMA sequence per n-tile
+                                    MmaOp<T>::run((jj & 1) ? sc2[nt] : sc[nt], a, b0, b1);
+                                }
+                            }
+                            sc[nt][0] += sc2[nt][0]; sc[nt][1] += sc2[nt][1];
+                            sc[nt][2] += sc2[nt][2]; sc[nt][3] += sc2[nt][3];
+                        }
+                    } else {
+                        if (valid < kRows) {
+                            // rows past the sequence may hold anything (even NaN): zero them in
+                            // V so that 0 * row stays 0 inside the MMA
+                            uint8_t* vgen = smem + (vbase - smem_u32(smem));
+                            const int nbytes = (kRows - valid) * 128;
+                            for (int hx = 0; hx < kHalves; ++hx)
+                                for (int off = lane * 16; off < nbytes; off += 32 * 16)
+                                    *reinterpret_cast<uint4*>(vgen + hx * kHalfTile + valid * 128 + off) =
+                                        make_uint4(0, 0, 0, 0);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        // S = Q K^T for the 16 rows
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+                            for (int kc = 0; kc < D / 16; kc += 2) {
+                                const int r = nt * 8 + (lane & 7);
+                                const int chunk = kc * 2 + (lane >> 3);
+                                const uint32_t addr = kbase + (chunk >> 3) * kHalfTile + r * 128 +
+                                                      (((chunk & 7) ^ (r & 7)) << 4);
+                                uint32_t b0, b1, b2, b3;
+                                ldsm_x4(addr, b0, b1, b2, b3);
+                                const uint32_t a0[4] = {qa[kc][0], R16 ? qb[R16 ? kc : 0][0] : 0u, qa[kc][1],
+                                                        R16 ? qb[R16 ? kc : 0][1] : 0u};
+                                const uint32_t a1[4] = {qa[kc + 1][0], R16 ? qb[R16 ? kc + 1 : 0][0] : 0u,
+                                                        qa[kc + 1][1], R16 ? qb[R16 ? kc + 1 : 0][1] : 0u};
+                                MmaOp<T>::run(sc[nt], a0, b0, b1);
+                                MmaOp<T>::run(sc[nt], a1, b2, b3);
+                            }
                         }
                     }
-                }
 
-                // online softmax on row g (log2 domain)
-                float mx = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int p = pos0 + (FP8 ? 4 * t4 + 2 * nt + e : nt * 8 + 2 * t4 + e);
-                        const float z = p < lim ? sc[nt][e] * row_l2 : -INFINITY;
-                        sc[nt][e] = z;
-                        mx = fmaxf(mx, z);
-                    }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run, mx);
-                // a row with no visible key so far (several queries per sequence)
-                // keeps m = -inf: exponents are then taken against 0, giving 0
-                const float m_use = (MQ && m_new == -INFINITY) ? 0.f : m_new;
-                float m_new1 = -INFINITY, m_use1 = 0.f;
-                if constexpr (R16) {   // the second row of this thread, same steps
-                    float mx1 = -INFINITY;
+                    // online softmax on row g (log2 domain)
+                    float mx = -INFINITY;
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int e = 2; e < 4; ++e) {
-                            const int p = pos0 + nt * 8 + 2 * t4 + e - 2;
-                            const float z = p < lim1 ? sc[nt][e] * scale_log2 : -INFINITY;
+                        for (int e = 0; e < 2; ++e) {
+                            const int p = pos0 + (FP8 ? 4 * t4 + 2 * nt + e : nt * 8 + 2 * t4 + e);
+                            const float z = p < lim ? sc[nt][e] * row_l2 : -INFINITY;
                             sc[nt][e] = z;
-                            mx1 = fmaxf(mx1, z);
+                            mx = fmaxf(mx, z);
                         }
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                    m_new1 = fmaxf(m_run1, mx1);
-                    m_use1 = m_new1 == -INFINITY ? 0.f : m_new1;
-                }
-                // rescale only when some row's running max moved (warp-uniform
-                // branch; after the first stages the max rarely moves).  The first
-                // stage has m_run = -inf: alpha = 0 clears the (zero) state.
-                if (__any_sync(0xffffffffu, m_new != m_run || (R16 && m_new1 != m_run1))) {
-                    const float alpha = fast_exp2(m_run - m_use);
-                    const float alpha1 = R16 ? fast_exp2(m_run1 - m_use1) : alpha;
-                    l_run *= alpha;
-                    l_run1 *= alpha1;
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_new = fmaxf(m_run, mx);
+                    // a row with no visible key so far (several queries per sequence)
+                    // keeps m = -inf: exponents are then taken against 0, giving 0
+                    const float m_use = (MQ && m_new == -INFINITY) ? 0.f : m_new;
+                    float m_new1 = -INFINITY, m_use1 = 0.f;
+                    if constexpr (R16) {   // the second row of this thread, same steps
+                        float mx1 = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < D / 8; ++i) {
-                        o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha1; o[i][3] *= alpha1;
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 2; e < 4; ++e) {
+                                const int p = pos0 + nt * 8 + 2 * t4 + e - 2;
+                                const float z = p < lim1 ? sc[nt][e] * scale_log2 : -INFINITY;
+                                sc[nt][e] = z;
+                                mx1 = fmaxf(mx1, z);
+                            }
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                        m_new1 = fmaxf(m_run1, mx1);
+                        m_use1 = m_new1 == -INFINITY ? 0.f : m_new1;
                     }
-                }
-                m_run = m_new;
-                m_run1 = m_new1;
-                float psum = 0.f, psum1 = 0.f;
+                    // rescale only when some row's running max moved (warp-uniform
+                    // branch; after the first stages the max rarely moves).  The first
+                    // stage has m_run = -inf: alpha = 0 clears the (zero) state.
+                    if (__any_sync(0xffffffffu, m_new != m_run || (R16 && m_new1 != m_run1))) {
+                        const float alpha = fast_exp2(m_run - m_use);
+                        const float alpha1 = R16 ? fast_exp2(m_run1 - m_use1) : alpha;
+                        l_run *= alpha;
+                        l_run1 *= alpha1;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < (R16 ? 4 : 2); ++e) {
-                        const float p = fast_exp2(sc[nt][e] - (e < 2 ? m_use : m_use1));
-                        sc[nt][e] = p;
-                        if (e < 2) psum += p; else psum1 += p;
+                        for (int i = 0; i < D / 8; ++i) {
+                            o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha1; o[i][3] *= alpha1;
+                        }
                     }
-                l_run += psum;
-                l_run1 += psum1;
+                    m_run = m_new;
+                    m_run1 = m_new1;
+                    float psum = 0.f, psum1 = 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < (R16 ? 4 : 2); ++e) {
+                            const float p = fast_exp2(sc[nt][e] - (e < 2 ? m_use : m_use1));
+                            sc[nt][e] = p;
+                            if (e < 2) psum += p; else psum1 += p;
+                        }
+                    l_run += psum;
+                    l_run1 += psum1;
 
-                // O += P V, P as hi (rows 0-7) + lo (rows 8-15); RU 16: rows g and
-                // g + 8 both real, hi in pa and lo in pb, two MMAs
-                uint32_t pa[4], pb[4];
-                if constexpr (R16) {
-                    split_pair<T>(sc[0][0], sc[0][1], pa[0], pb[0]);
-                    split_pair<T>(sc[0][2], sc[0][3], pa[1], pb[1]);
-                    split_pair<T>(sc[1][0], sc[1][1], pa[2], pb[2]);
-                    split_pair<T>(sc[1][2], sc[1][3], pa[3], pb[3]);
-                } else {
-                    split_pair<T>(sc[0][0], sc[0][1], pa[0], pa[1]);
-                    split_pair<T>(sc[1][0], sc[1][1], pa[2], pa[3]);
-                }
-                if constexpr (FP8) {
-                    // transposed V tile: row d holds tokens 0..15; a fragment word is
-                    // tokens 4*t4 .. 4*t4+3 of row d, the k order P is in
+                    // O += P V, P as hi (rows 0-7) + lo (rows 8-15); RU 16: rows g and
+                    // g + 8 both real, hi in pa and lo in pb, two MMAs
+                    uint32_t pa[4], pb[4];
+                    if constexpr (R16) {
+                        split_pair<T>(sc[0][0], sc[0][1], pa[0], pb[0]);
+                        split_pair<T>(sc[0][2], sc[0][3], pa[1], pb[1]);
+                        split_pair<T>(sc[1][0], sc[1][1], pa[2], pb[2]);
+                        split_pair<T>(sc[1][2], sc[1][3], pa[3], pb[3]);
+                    } else {
+                        split_pair<T>(sc[0][0], sc[0][1], pa[0], pa[1]);
+                        split_pair<T>(sc[1][0], sc[1][1], pa[2], pa[3]);
+                    }
+                    if constexpr (FP8) {
+                        // transposed V tile: row d holds tokens 0..15; a fragment word is
+                        // tokens 4*t4 .. 4*t4+3 of row d, the k order P is in
 #pragma unroll
-                    for (int nd = 0; nd < D / 8; nd += 4) {
-                        const int d_row = (nd + (lane >> 3)) * 8 + (lane & 7);
-                        uint32_t w[4];
-                        ldsm_x4(vbase + d_row * 16, w[0], w[1], w[2], w[3]);
+                        for (int nd = 0; nd < D / 8; nd += 4) {
+                            const int d_row = (nd + (lane >> 3)) * 8 + (lane & 7);
+                            uint32_t w[4];
+                            ldsm_x4(vbase + d_row * 16, w[0], w[1], w[2], w[3]);
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                        {
-                            uint32_t b0, b1;
-                            e4m3x4_to_h2x2(w[jj], b0, b1);
-                            MmaOp<T>::run(o[nd + jj], pa, b0, b1);
+                            for (int jj = 0; jj < 4; ++jj)
+                            {
+                                uint32_t b0, b1;
+                                e4m3x4_to_h2x2(w[jj], b0, b1);
+                                MmaOp<T>::run(o[nd + jj], pa, b0, b1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int nt = 0; nt < D / 8; nt += 2) {
+                            const int mi = lane >> 3;
+                            const int r = (mi & 1) * 8 + (lane & 7);
+                            const int chunk = nt + (mi >> 1);
+                            const uint32_t addr = vbase + (chunk >> 3) * kHalfTile + r * 128 +
+                                                  (((chunk & 7) ^ (r & 7)) << 4);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_t(addr, b0, b1, b2, b3);
+                            MmaOp<T>::run(o[nt], pa, b0, b1);
+                            MmaOp<T>::run(o[nt + 1], pa, b2, b3);
+                            if constexpr (R16) {
+                                MmaOp<T>::run(o[nt], pb, b0, b1);
+                                MmaOp<T>::run(o[nt + 1], pb, b2, b3);
+                            }
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int nt = 0; nt < D / 8; nt += 2) {
-                        const int mi = lane >> 3;
-                        const int r = (mi & 1) * 8 + (lane & 7);
-                        const int chunk = nt + (mi >> 1);
-                        const uint32_t addr = vbase + (chunk >> 3) * kHalfTile + r * 128 +
-                                              (((chunk & 7) ^ (r & 7)) << 4);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(addr, b0, b1, b2, b3);
-                        MmaOp<T>::run(o[nt], pa, b0, b1);
-                        MmaOp<T>::run(o[nt + 1], pa, b2, b3);
-                        if constexpr (R16) {
-                            MmaOp<T>::run(o[nt], pb, b0, b1);
-                            MmaOp<T>::run(o[nt + 1], pb, b2, b3);
-                        }
-                    }
-                }
 
+                }
                 __syncwarp();
                 if (lane == 0 && k + NS < my_n) {
                     fence_proxy_async_smem();
@@ -670,35 +817,27 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             kt += my_n;
             // ---- this warp's share of the combine
-            l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-            l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-            if constexpr (R16) {
-                l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 1);
-                l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 2);
-            }
-            if constexpr (Cfg::kSepRed) {
+            if constexpr (kTr) {
+                // column sums over the eight lanes of each t4; a head's hi and lo
+                // columns (t4 and t4 + 2) add up
 #pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt) {
-                    float* dst = red_o + (warp * RU + g) * D + nt * 8 + 2 * t4;
-                    if constexpr (R16) {
-                        dst[0] = o[nt][0];
-                        dst[1] = o[nt][1];
-                        dst[8 * D] = o[nt][2];           // row g + 8
-                        dst[8 * D + 1] = o[nt][3];
-                    } else {
-                        dst[0] = o[nt][0] + o[nt][2];
-                        dst[1] = o[nt][1] + o[nt][3];
-                    }
+                for (int w = 4; w < 32; w <<= 1) {
+                    l_run += __shfl_xor_sync(0xffffffffu, l_run, w);
+                    l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, w);
                 }
-                if (t4 == 0) {
-                    red_m[warp * RU + g] = m_run;
-                    red_l[warp * RU + g] = l_run;
-                    if constexpr (R16) {
-                        red_m[warp * RU + g + 8] = m_run1;
-                        red_l[warp * RU + g + 8] = l_run1;
-                    }
+#pragma unroll
+                for (int mt = 0; mt < kOT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
+            } else {
+                l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+                l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+                if constexpr (R16) {
+                    l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 1);
+                    l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 2);
                 }
             }
+            if constexpr (Cfg::kSepRed) write_partials();
         }
         if (nx.live && tid < nx.nblk) s_blk[cb ^ 1][tid] = nb_id;
         if (MQ && cu.live && tid < nh) {
@@ -717,27 +856,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (cu.live) {
             if constexpr (!Cfg::kSepRed) {
                 // the combine buffer aliases the rings: written after the barrier
-#pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt) {
-                    float* dst = red_o + (warp * RU + g) * D + nt * 8 + 2 * t4;
-                    if constexpr (R16) {
-                        dst[0] = o[nt][0];
-                        dst[1] = o[nt][1];
-                        dst[8 * D] = o[nt][2];           // row g + 8
-                        dst[8 * D + 1] = o[nt][3];
-                    } else {
-                        dst[0] = o[nt][0] + o[nt][2];
-                        dst[1] = o[nt][1] + o[nt][3];
-                    }
-                }
-                if (t4 == 0) {
-                    red_m[warp * RU + g] = m_run;
-                    red_l[warp * RU + g] = l_run;
-                    if constexpr (R16) {
-                        red_m[warp * RU + g + 8] = m_run1;
-                        red_l[warp * RU + g + 8] = l_run1;
-                    }
-                }
+                write_partials();
                 fence_proxy_async_smem();   // these generic writes precede later TMA writes here
                 __syncthreads();
             }
@@ -903,6 +1022,16 @@ template <typename QT, bool MQ>
 cudaError_t run_fp8_qt(const DecodeArgs& a, cudaStream_t s, float sl2)
 {
     const int D = a.cache.head_dim, BS = a.cache.block_size;
+    if constexpr (!MQ) {
+        // up to 4 query heads a KV head: the transposed kernel (4-row units)
+        if (a.n_q / a.cache.n_kv_heads <= 4) {
+            if (D == 64 && BS == 16) return run_mma<__half, QT, 64, 16, true, false, 4>(a, s, sl2);
+            if (D == 64 && BS == 32) return run_mma<__half, QT, 64, 32, true, false, 4>(a, s, sl2);
+            if (D == 128 && BS == 16) return run_mma<__half, QT, 128, 16, true, false, 4>(a, s, sl2);
+            if (D == 128 && BS == 32) return run_mma<__half, QT, 128, 32, true, false, 4>(a, s, sl2);
+            return cudaErrorNotSupported;
+        }
+    }
     if (D == 64 && BS == 16) return run_mma<__half, QT, 64, 16, true, MQ>(a, s, sl2);
     if (D == 64 && BS == 32) return run_mma<__half, QT, 64, 32, true, MQ>(a, s, sl2);
     if (D == 128 && BS == 16) return run_mma<__half, QT, 128, 16, true, MQ>(a, s, sl2);

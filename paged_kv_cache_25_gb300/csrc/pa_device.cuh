@@ -169,6 +169,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "r"(addr));
 }
 
+// Transpose of an 8 x 8 matrix of 16-bit elements held across the warp in
+// the MMA fragment layout (lane 4*r + c holds elements (r, 2c) and (r, 2c + 1)):
+// afterwards lane 4*r + c holds elements (2c, r) and (2c + 1, r).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 template <typename T> struct MmaOp;
 
 template <> struct MmaOp<__nv_bfloat16> {
