@@ -42,16 +42,16 @@ FALLBACK_HBM_GBS = 6800.0
 # K/V bytes of the captured launch, what was captured); a record of another
 # batch of the same workload is scaled by its unique K/V bytes.
 NCU_TRAFFIC = {
-    ("llama3-8b-bf16", "8c018e5e71f5b98c"): (2372009472 + 13484800, 2359717888,
+    ("llama3-8b-bf16", "058a5c702984a9c9"): (2372048640 + 13103360, 2359717888,
                                              "full 256-sequence batch, one-pass capture"),
-    ("llama3-8b-fp8", "8c018e5e71f5b98c"): (1188431360 + 14343936, 1179858944,
+    ("llama3-8b-fp8", "058a5c702984a9c9"): (1188178944 + 12511744, 1179858944,
                                             "full 256-sequence batch, one-pass capture"),
 }
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
 # chunks as the 60 GB pool): bytes per launch
 NCU_PREFILL_TRAFFIC = {
-    ("mixed-llama3-8b-bf16", "2d38b48613ecaf60"): (98304256 + 4817664, "compact pool, --set full"),
-    ("mixed-llama3-8b-fp8", "2d38b48613ecaf60"): (57562368 + 1563136, "compact pool, --set full"),
+    ("mixed-llama3-8b-bf16", "b13ead73ea0e5356"): (98299392 + 4567808, "compact pool, --set full"),
+    ("mixed-llama3-8b-fp8", "b13ead73ea0e5356"): (57555712 + 1308416, "compact pool, --set full"),
 }
 
 

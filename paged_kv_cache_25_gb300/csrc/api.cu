@@ -110,13 +110,15 @@ int decode_partition_tokens(int64_t seq_groups, int block_size, int max_context_
     // 1024 tokens (64 or 32 blocks) per partition spreads the fixed cost of a
     // unit (block ids, q fragments, the first TMA round trip, the cross-warp
     // combine) over 16 stages per warp and keeps the split-K bytes below 1 %;
-    // halve it (down to 128) while the batch would offer fewer than ~2 units
-    // of work per resident CTA (2 per SM on 152 SMs): the work counter and the
-    // next-unit prefetch balance the rest (a 64-sequence TinyLlama-shaped
-    // batch: 32.6 us at a bound of 8 units per CTA, 27.0 us at 2).
+    // halve it (down to 128) while the batch would offer fewer than ~300 units
+    // (about one per resident CTA at 2 per SM on 152 SMs): smaller units cost
+    // more in per-unit overhead and split-K traffic than they win in balance
+    // (a 64-sequence TinyLlama-shaped batch, 3 CTAs per SM: the decode kernel
+    // at 0.378 of the copy peak with a bound of 608 units, 0.394 with 300,
+    // 0.340 with 1216).
     int p = 1024;
     while (p > 128 && p > block_size &&
-           seq_groups * ((max_context_len + p - 1) / p) < 608)
+           seq_groups * ((max_context_len + p - 1) / p) < 300)
         p /= 2;
     return p;
 }
