@@ -632,10 +632,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 tmem_ld_wait();
                 if (full_tile) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sa[i]));
-                        m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sb[i]));
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        m4[i & 3] = max3f(m4[i & 3], __uint_as_float(sa[i]), __uint_as_float(sb[i]));
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -682,6 +680,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             // written over those 32 keys' own score columns (hi in the first
             // 16, lo in the next 16), so no score is overwritten before it is read
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // full tiles
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 uint32_t sr[32];
@@ -689,13 +688,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 tmem_ld_wait();
                 uint32_t ph[16], pl[16];
                 if (full_tile) {
+                    // pairs of keys in paired fp32 instructions: the exponent's
+                    // argument, the row sum and P's lo residual
+                    const float2 c2 = make_float2(scale_log2, scale_log2), n2 = make_float2(neg_mc, neg_mc);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), scale_log2, neg_mc));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), scale_log2, neg_mc));
-                        s4[i & 3] += p0 + p1;
-                        if constexpr (kOneP) ph[i] = Cvt<__half>::pack(p0, p1);
-                        else split_trunc<T>(p0, p1, ph[i], pl[i]);
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                              c2, n2);
+                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        s2[i & 1] = add2(s2[i & 1], pp);
+                        if constexpr (kOneP) {
+                            ph[i] = Cvt<__half>::pack(pp.x, pp.y);
+                        } else {
+                            // hi: the upper 16 bits of each (truncation); lo: the exact
+                            // remainder, rounded to bf16
+                            const uint32_t u0 = __float_as_uint(pp.x), u1 = __float_as_uint(pp.y);
+                            ph[i] = __byte_perm(u0, u1, 0x7632);
+                            const float2 r = sub2(pp, make_float2(__uint_as_float(u0 & 0xFFFF0000u),
+                                                                  __uint_as_float(u1 & 0xFFFF0000u)));
+                            pl[i] = Cvt<T>::pack(r.x, r.y);
+                        }
                     }
                 } else {   // masked keys give exactly 0 (even with scale 0, where -inf * 0 is NaN)
 #pragma unroll
@@ -712,7 +724,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if constexpr (!kOneP) tmem_st16(lane_addr + s_col + h2 * 32 + 16, pl);   // just read
 
             }
-            l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            l += ((s4[0] + s4[1]) + (s4[2] + s4[3])) + ((s2[0].x + s2[0].y) + (s2[1].x + s2[1].y));
             tmem_st_wait();
 
             if (!F8 && key0 + kTcKeys > L) {   // FP8: the producers wrote zeros there
