@@ -139,6 +139,17 @@ CASES = [
 ]
 
 
+TRANSPOSED_CASES = [
+    # up to 4 query heads a KV head run the transposed kernel: every group
+    # size 1-4 with both head dims and both block sizes among them
+    (5, 3, 8, 4, 128, 32, torch.bfloat16, [2, 1023, 1500], 1.0 / 64),   # g=2
+    (6, 4, 12, 4, 64, 32, torch.float16, [17, 32, 800, 2100], 0.0125),  # g=3
+    (7, 3, 12, 3, 128, 16, torch.bfloat16, [48, 1, 3000], 1.0 / 64),    # g=4, 3 KV heads
+    (8, 2, 6, 6, 64, 32, torch.bfloat16, [5000, 31], 1.0 / 64),         # g=1, d 64, bs 32
+]
+CASES = CASES + TRANSPOSED_CASES
+
+
 @pytest.mark.parametrize("case", CASES, ids=[f"f{c[0]}" for c in CASES])
 def test_fp8_decode_matches_oracle_on_dequantized_kv(case):
     seed, B, n_q, n_kv, d, bs, act, lens, scale = case
