@@ -410,6 +410,19 @@ __device__ __forceinline__ void umma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tm
         : "memory");
 }
 
+// kind::f8f6f4 from a converged warp, A and B (8-bit codes) in shared memory
+__device__ __forceinline__ void umma_f8_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // commit from the elected lane (the lane that issued the warp's MMAs)
 __device__ __forceinline__ void umma_commit_elect(uint32_t mbar)
 {

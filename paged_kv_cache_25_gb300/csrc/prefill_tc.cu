@@ -53,16 +53,29 @@ constexpr int kTcKeys = 128;      // keys per key tile
 constexpr int kTcStages = 2;      // K/V ring depth
 constexpr int kSoftmaxWarps = 8 * kTcTiles;   // two threads per row of each tile
 constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1;
-// FP8 pools: warps that widen codes into the rings.  A key tile is 2 x
-// (128 / kF8ChunkKeys) chunks (K's, then V's); chunk g of the whole sequence
-// goes to converter g % kF8Converters.
-constexpr int kF8Converters = 3;
+// FP8 pools: three warps widen codes into the rings.  In general a key tile
+// is 2 x (128 / kF8ChunkKeys) chunks (K's, then V's) and chunk g of the whole
+// sequence goes to converter g % 3.  With head_dim 128 and bf16 queries the
+// score MMA reads the K codes as they are (kind::f8f6f4; each q row, scaled by
+// a power of two, is exactly the sum of two E4M3 parts): the MMA warp loads
+// the codes by TMA a key tile ahead and the converters widen V alone.  (An
+// fp16 query has 11 significant bits, more than two E4M3 parts carry.)
 constexpr int kF8ChunkKeys = 32;   // keys per staged chunk of codes (16 or 32)
-// Warps after the softmax ones: the K and V producers (or FP8 converters),
-// then the MMA issuer.
-template <bool F8>
+constexpr int kF8MaxConverters = 3;
+constexpr int kF8MaxDepth = 2;     // staging buffers per converter
+template <bool F8, int D, bool BQ>
+struct PfMode {
+    static constexpr bool kDirectK = F8 && D == 128 && BQ;   // K codes straight into the score MMA
+    static constexpr int kConverters = F8 ? 3 : 0;
+    static constexpr int kDepth = 2;
+};
+// Warps after the softmax ones: the K and V producers (or the FP8
+// converters), then the MMA issuer.
+template <bool F8, int D, bool BQ>
 struct PfWarps {
-    static constexpr int kProducers = F8 ? kF8Converters : 2;
+    using Mode = PfMode<F8, D, BQ>;
+    static constexpr int kProducers = F8 ? Mode::kConverters : 2;
+    static constexpr int kFirstConverter = kSoftmaxWarps;
     static constexpr int kMma = kSoftmaxWarps + kProducers;
     static constexpr int kThreads = (kMma + 1) * 32;
     // the register file is split per SM sub-partition: 20 warps (5 on each)
@@ -71,17 +84,22 @@ struct PfWarps {
 };
 constexpr uint32_t kTmemCols = 512;   // S/P_A [0,128) S/P_B [128,256) O_A, O_B from 256
 
-template <typename T, int D, bool F8 = false>
+template <typename T, int D, bool F8, bool BQ>
 struct PfLayout {
+    static constexpr bool kDirectK = PfMode<F8, D, BQ>::kDirectK;
     static constexpr int kHalves = D / 64;
-    static constexpr uint32_t kQBytes = kTcRows * D * 2;          // one Q tile
-    static constexpr uint32_t kKBytes = kTcKeys * D * 2;          // K (or V) of one key tile
+    // one Q tile: 16-bit rows, or (direct K) the E4M3 hi part then the lo part
+    static constexpr uint32_t kQBytes = kTcRows * D * 2;
+    static constexpr uint32_t kQLo = kTcRows * D;                 // direct K: offset of the lo part
+    static constexpr uint32_t kKBytes = kTcKeys * D * (kDirectK ? 1 : 2);   // K of one key tile
+    static constexpr uint32_t kVBytes = kTcKeys * D * 2;          // V of one key tile (16-bit)
     static constexpr uint32_t kCodeBytes = kF8ChunkKeys * D;      // FP8: codes of one staged chunk
     static constexpr uint32_t kOffQ = 0;                          // Q_A, Q_B
     static constexpr uint32_t kOffK = kOffQ + kTcTiles * kQBytes; // K ring
     static constexpr uint32_t kOffV = kOffK + kTcStages * kKBytes;   // V ring
-    static constexpr uint32_t kOffCS = kOffV + kTcStages * kKBytes;  // FP8: 2 code buffers per converter
-    static constexpr uint32_t kDynBytes = kOffCS + (F8 ? kF8Converters * 2 * kCodeBytes : 0) + 1024;
+    static constexpr uint32_t kOffCS = kOffV + kTcStages * kVBytes;  // FP8: 2 code buffers per converter
+    static constexpr uint32_t kDynBytes =
+        kOffCS + PfMode<F8, D, BQ>::kConverters * PfMode<F8, D, BQ>::kDepth * kCodeBytes + 1024;
     // S_t at t * 128; P_t overwrites it, keys 32c .. 32c+31 as hi in columns
     // 32c .. 32c+15 and (bf16 operands) lo in 32c+16 .. 32c+31 (two 16-bit
     // values per column)
@@ -153,7 +171,7 @@ __device__ __forceinline__ uint4 keep_codes(uint4 c, int keep)
 // scaled by a power of two 2^-e into fp16 (exact for bf16 values down to 2^-28
 // of the row's largest) and 2^e goes into that row's softmax scale.
 template <typename T, typename QT, int D, int BS, bool F8 = false>
-__global__ void __launch_bounds__(PfWarps<F8>::kThreads, 1)
+__global__ void __launch_bounds__(PfWarps<F8, D, std::is_same<QT, __nv_bfloat16>::value>::kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const uint8_t* __restrict__ k_codes, const uint8_t* __restrict__ v_codes,
                   void* __restrict__ out, pa_dtype out_dtype, const QT* __restrict__ q,
@@ -162,8 +180,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                   int max_q, int n_q, int n_kv, int group, int num_blocks, float scale_log2,
                   float v_scale, unsigned* err)
 {
-    using Ly = PfLayout<T, D, F8>;
-    constexpr int kMmaWarp = PfWarps<F8>::kMma;
+    constexpr bool kBq = std::is_same<QT, __nv_bfloat16>::value;
+    using Ly = PfLayout<T, D, F8, kBq>;
+    using Wp = PfWarps<F8, D, kBq>;
+    constexpr bool kDirectK = Ly::kDirectK;
+    constexpr int kMmaWarp = Wp::kMma;
+    constexpr int kFirstConv = Wp::kFirstConverter;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     // P for P V: fp16 operands (fp16 and FP8 pools) take P as one fp16 part,
     // 11 significant bits, so each output moves by at most 2^-12 of the
@@ -171,6 +193,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // (8 significant bits each, ~16 together)
     constexpr bool kOneP = !kBf16;
     constexpr uint32_t kIdescQK = idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
+    // kind::f8f6f4 with E4M3 A and B (type code 0 in both fields), fp32 accumulate
+    constexpr uint32_t kIdescQK8 = idesc_f16(false, false, false, kTcRows, kTcKeys);
     // P V: V as [keys][d] (MN-major) from 16-bit pools, as [d][keys] (K-major) from FP8
     constexpr uint32_t kIdescPV = idesc_f16(kBf16, false, !F8, kTcRows, D);
     static_assert(BS % 16 == 0 && kTcKeys % BS == 0, "block size must divide the key tile");
@@ -208,7 +232,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     __shared__ __align__(8) uint64_t k_full[kTcStages], k_empty[kTcStages];
     __shared__ __align__(8) uint64_t v_full[kTcStages], v_empty[kTcStages];
     __shared__ __align__(8) uint64_t s_full[kTcTiles], p_full[kTcTiles], pv_done[kTcTiles], q_ready;
-    __shared__ __align__(8) uint64_t code_full[kF8Converters][2];   // FP8: codes landed, per converter and buffer
+    __shared__ __align__(8) uint64_t code_full[kF8MaxConverters][kF8MaxDepth];   // FP8: codes landed, per converter and buffer
     __shared__ uint32_t s_tmem;
     // partial row maxima of the two threads of a row (double-buffered by key
     // tile), a "stop" flag beside each, and the partial row sums at the end
@@ -224,8 +248,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < kTcStages; ++i) {
-            // FP8: one arrival per widened chunk; 16-bit pools: the TMA's
-            mbar_init(smem_u32(&k_full[i]), F8 ? kTcKeys / kF8ChunkKeys : 1);
+            // FP8: one arrival per widened chunk; 16-bit pools and the direct
+            // K codes: the TMA's
+            mbar_init(smem_u32(&k_full[i]), F8 && !kDirectK ? kTcKeys / kF8ChunkKeys : 1);
             mbar_init(smem_u32(&k_empty[i]), 1);
             mbar_init(smem_u32(&v_full[i]), F8 ? kTcKeys / kF8ChunkKeys : 1);
             mbar_init(smem_u32(&v_empty[i]), 1);
@@ -236,7 +261,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             mbar_init(smem_u32(&pv_done[t]), 1);
         }
         mbar_init(smem_u32(&q_ready), kSoftmaxWarps);
-        for (int i = 0; i < 2 * kF8Converters; ++i) mbar_init(smem_u32(&code_full[i >> 1][i & 1]), 1);
+        for (int i = 0; i < kF8MaxDepth * kF8MaxConverters; ++i)
+            mbar_init(smem_u32(&code_full[i / kF8MaxDepth][i % kF8MaxDepth]), 1);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
@@ -249,21 +275,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t tmem = s_tmem;
 
     static_assert(!F8 || std::is_same<T, __half>::value, "FP8 codes widen to fp16 operands");
-    if (F8 && warp >= kSoftmaxWarps && warp < kMmaWarp) {
+    if (F8 && warp >= kFirstConv && warp < kMmaWarp) {
         // ------------------------------------------------ FP8 converters
-        // Chunk g (tile g / (2 kChunks); K chunks first, then V) is widened by
-        // converter g % kF8Converters into its ring stage, which then gets
+        // Chunk g (tile g / kPerTile; K chunks first, then V) is widened by
+        // converter g % kNc into its ring stage, which then gets
         // one arrival on its full barrier.  Each converter's chunks pass
-        // through two staging buffers: while it widens its chunk n, chunk n + 1
-        // is in flight, and lane 0 requests chunk n + 2 into the same buffer
-        // once the warp has read it.  The block ids of a tile's 16-key pieces
+        // through kDepth staging buffers: while it widens its chunk n, chunks
+        // n + 1 .. n + kDepth - 1 are in flight, and lane 0 requests chunk
+        // n + kDepth into the same buffer once the warp has read it (the chunk
+        // is at most two key tiles ahead).  The block ids of a tile's 16-key pieces
         // (one per lane) are loaded a tile ahead.
+        // (direct K: V chunks only)
         constexpr int kCK = kF8ChunkKeys, kChunks = kTcKeys / kCK, kBoxes = kCK / 16;
-        constexpr int kPerTile = 2 * kChunks, kNc = kF8Converters;
-        const int pw = warp - kSoftmaxWarps;
+        constexpr int kKChunks = kDirectK ? 0 : kChunks;       // K chunks per tile
+        constexpr int kPerTile = kKChunks + kChunks;
+        constexpr int kNc = F8 ? Wp::Mode::kConverters : 1;     // (16-bit pools never get here)
+        constexpr int kDepth = Wp::Mode::kDepth;
+        const int pw = warp - kFirstConv;
         const int total = (kPerTile * n_tiles - pw + kNc - 1) / kNc;   // this warp's chunks
-        const uint32_t stage = sbase + Ly::kOffCS + pw * 2 * Ly::kCodeBytes;
-        const uint8_t* stage_ptr = smem + Ly::kOffCS + pw * 2 * Ly::kCodeBytes;
+        const uint32_t stage = sbase + Ly::kOffCS + pw * kDepth * Ly::kCodeBytes;
+        const uint8_t* stage_ptr = smem + Ly::kOffCS + pw * kDepth * Ly::kCodeBytes;
         const uint64_t* cbars = code_full[pw];
         const int32_t* table = block_tables + static_cast<int64_t>(r) * max_blocks;
         // lane c < 8: raw block id of 16-key piece c of tile t (-1: past the
@@ -278,15 +309,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         int ids[2] = {piece_ids(0), piece_ids(1)};
         auto request = [&](int n) {   // whole warp: this warp's chunk n
             const int g = pw + kNc * n, j = g / kPerTile, item = g % kPerTile;
-            const bool k_chunk = item < kChunks;
-            const int e = k_chunk ? item : item - kChunks;
+            const bool k_chunk = item < kKChunks;
+            const int e = k_chunk ? item : item - kKChunks;
             const int src_ids = j == id_tile ? ids[0] : ids[1];   // j <= id_tile + 1
             int bb[kBoxes];
 #pragma unroll
             for (int x = 0; x < kBoxes; ++x) bb[x] = __shfl_sync(0xffffffffu, src_ids, e * kBoxes + x);
             if (lane == 0) {
-                const uint32_t bar = smem_u32(&cbars[n & 1]);
-                const uint32_t buf = stage + (n & 1) * Ly::kCodeBytes;
+                const uint32_t bar = smem_u32(&cbars[n % kDepth]);
+                const uint32_t buf = stage + (n % kDepth) * Ly::kCodeBytes;
                 mbar_arrive_expect_tx(bar, Ly::kCodeBytes);
 #pragma unroll
                 for (int x = 0; x < kBoxes; ++x) {
@@ -309,15 +340,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // on a wait that ran out (error recorded): let the copies of chunks n
         // and n + 1 land (bounded) before the CTA can exit
         auto drain = [&](int n) {
-            for (int m = n; m < min(n + 2, total); ++m)
-                mbar_wait(smem_u32(&cbars[m & 1]), (m >> 1) & 1, err);
+            for (int m = n; m < min(n + kDepth, total); ++m)
+                mbar_wait(smem_u32(&cbars[m % kDepth]), (m / kDepth) & 1, err);
         };
-        for (int n = 0; n < min(2, total); ++n) request(n);
+        for (int n = 0; n < min(kDepth, total); ++n) request(n);
 #pragma unroll 1
         for (int n = 0; n < total; ++n) {
             const int g = pw + kNc * n, j = g / kPerTile, item = g % kPerTile;
-            const bool k_chunk = item < kChunks;
-            const int e = k_chunk ? item : item - kChunks;
+            const bool k_chunk = item < kKChunks;
+            const int e = k_chunk ? item : item - kKChunks;
             const int st = j % kTcStages;
             if (j >= kTcStages &&
                 !__all_sync(0xffffffffu, mbar_wait(smem_u32(&(k_chunk ? k_empty : v_empty)[st]),
@@ -325,18 +356,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 drain(n);
                 break;
             }
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&cbars[n & 1]), (n >> 1) & 1, err))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&cbars[n % kDepth]), (n / kDepth) & 1, err))) {
                 drain(n);
                 break;
             }
-            const uint32_t dst = sbase + (k_chunk ? Ly::kOffK : Ly::kOffV) + st * Ly::kKBytes;
+            const uint32_t dst = k_chunk ? sbase + Ly::kOffK + st * Ly::kKBytes
+                                         : sbase + Ly::kOffV + st * Ly::kVBytes;
             const int keep_tile = L - j * kTcKeys;        // valid keys of this tile (may exceed 128)
             // kCK x D codes in units of 16: one K row's d-chunk pair p (or one
             // V^T row of a 16-key piece), each widened into two 16-byte ring
             // chunks.  Every 8 lanes touch 8 distinct 16-byte bank groups in
             // the staging reads and in the ring writes.
             constexpr int kPer = kCK * D / 512;
-            const uint8_t* src = stage_ptr + (n & 1) * Ly::kCodeBytes;
+            const uint8_t* src = stage_ptr + (n % kDepth) * Ly::kCodeBytes;
             uint4 c[kPer];
             int row[kPer], chunk0[kPer];
 #pragma unroll
@@ -393,17 +425,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             fence_proxy_async_smem();   // ring writes -> the MMAs' reads
             __syncwarp();               // and every lane has read the staging buffer
             if (lane == 0) mbar_arrive(smem_u32(&(k_chunk ? k_full : v_full)[st]));
-            if (n + 2 < total) {
-                const int jn = (pw + kNc * (n + 2)) / kPerTile;
+            if (n + kDepth < total) {
+                const int jn = (pw + kNc * (n + kDepth)) / kPerTile;
                 if (jn > id_tile + 1) {   // move the id window one tile on
                     id_tile += 1;
                     ids[0] = ids[1];
                     ids[1] = piece_ids(id_tile + 1);
                 }
-                request(n + 2);
+                request(n + kDepth);
             }
         }
-    } else if (warp == kKWarp || warp == kVWarp) {
+    } else if (!F8 && (warp == kKWarp || warp == kVWarp)) {
         // ------------------------------------------------ TMA producers
         // K and V have separate rings: K of key tile j is released once both
         // S_t(j) are done, V of tile j once both P_t(j) V are.
@@ -454,25 +486,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const uint64_t dv = F8 ? sdesc_sw128(sbase + Ly::kOffV, 16, 1024)
                                    : sdesc_sw128(sbase + Ly::kOffV, kTcKeys * 128, 1024);
             constexpr uint32_t kQHalf = (kTcRows * 128) >> 4, kKHalf = (kTcKeys * 128) >> 4;
-            constexpr uint32_t kKStage = Ly::kKBytes >> 4, kQTile = Ly::kQBytes >> 4;
+            constexpr uint32_t kKStage = Ly::kKBytes >> 4, kVStage = Ly::kVBytes >> 4;
+            constexpr uint32_t kQTile = Ly::kQBytes >> 4, kQLo = Ly::kQLo >> 4;
             // S_t(j) = Q_t K_j^T; the K stage is released after the last tile's
             auto issue_qk = [&](int t, int j) {
                 const int st = j % kTcStages;
                 const uint64_t dks = dk + st * kKStage;
                 const uint32_t d_s = tmem + Ly::kTmemS + t * 128;
                 const uint64_t dqt = dq + t * kQTile;
+                if constexpr (kDirectK) {
+                    // E4M3 x E4M3: 32 codes (32 bytes) per k-step of the one
+                    // 128-byte row; q's hi part, then its lo part, into S
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
-                    const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
-                    umma_f16_elect(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        umma_f8_elect(d_s, dqt + kk * 2, dks + kk * 2, kIdescQK8, kk > 0 ? 1u : 0u);
+                        umma_f8_elect(d_s, dqt + kQLo + kk * 2, dks + kk * 2, kIdescQK8, 1u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
+                        const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
+                        umma_f16_elect(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
+                    }
                 }
                 umma_commit_elect(smem_u32(&s_full[t]));
             };
             // O_t += P_t(j) V_j, P from TMEM (hi, and lo for bf16, of each 16 keys)
             auto issue_pv = [&](int t, int j) {
                 const int st = j % kTcStages;
-                const uint64_t dvs = dv + st * kKStage;
+                const uint64_t dvs = dv + st * kVStage;
                 const uint32_t d_o = tmem + Ly::kTmemO + t * D;
                 const uint32_t a_p = tmem + Ly::kTmemS + t * 128;
 #pragma unroll
@@ -494,6 +537,45 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, err));
             };
+            // Direct K (FP8 codes read by the score MMA): this warp loads key
+            // tile jt's codes into ring stage jt % 2, two tiles ahead of the
+            // scores that need them.  Lanes 0-7 look up the blocks of the tile's
+            // 16-key slabs a loop iteration early; lane 0 issues the boxes.
+            auto k_ids = [&](int jt) -> int {
+                if (!kDirectK || lane >= 8 || jt >= n_tiles) return 0;
+                // keys at or past L (masked in the softmax) read some block of the request
+                const int key = min(jt * kTcKeys + lane * 16, L - 1);
+                const int lb = key / BS;
+                return lb < max_blocks ? __ldg(block_tables + static_cast<int64_t>(r) * max_blocks + lb) : -1;
+            };
+            auto load_k = [&](int jt, int ids) {   // whole warp
+                int bb[kTcKeys / 16];
+#pragma unroll
+                for (int c = 0; c < kTcKeys / 16; ++c) bb[c] = __shfl_sync(0xffffffffu, ids, c);
+                if (lane == 0) {
+                    const uint32_t full = smem_u32(&k_full[jt % kTcStages]);
+                    const uint32_t dst = sbase + Ly::kOffK + (jt % kTcStages) * Ly::kKBytes;
+                    mbar_arrive_expect_tx(full, Ly::kKBytes);
+#pragma unroll
+                    for (int c = 0; c < kTcKeys / 16; ++c) {
+                        int b = bb[c];
+                        if (b < 0 || b >= num_blocks) {
+                            set_error(err, PA_ERR_OUT_OF_RANGE);
+                            b = 0;   // keep the ring moving; the outputs are flagged invalid
+                        }
+                        const int row = (b * n_kv + kvh) * BS + ((jt * kTcKeys + c * 16) % BS);
+                        tma_load_2d(dst + c * 2048, &kmap, 0, row, full);   // 16 rows x 128 codes
+                    }
+                }
+            };
+            int k_loaded = 0;   // direct K: key tiles requested so far
+            if constexpr (kDirectK) {
+                if (lane == 0) prefetch_tensormap(&kmap);
+                const int i0 = k_ids(0), i1 = k_ids(1);
+                load_k(0, i0);
+                if (n_tiles > 1) load_k(1, i1);
+                k_loaded = min(n_tiles, 2);
+            }
             bool ok = wait_all(&q_ready, 0) && wait_all(&k_full[0], 0);
             tc_fence_after();
             if (ok) {
@@ -504,6 +586,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % kTcStages, st1 = (j + 1) % kTcStages;
                 const bool more = j + 1 < n_tiles;
+                const int ids_ahead = k_ids(j + 2);   // direct K: blocks of tile j + 2
                 if (!wait_all(&v_full[st], (j / kTcStages) & 1)) break;
                 if (more && !wait_all(&k_full[st1], ((j + 1) / kTcStages) & 1)) break;
 #pragma unroll
@@ -520,7 +603,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if (!ok) break;
                 umma_commit_elect(smem_u32(&v_empty[st]));
                 if (more) umma_commit_elect(smem_u32(&k_empty[st1]));
+                if (kDirectK && j + 2 < n_tiles) {
+                    // stage st held K(j): free once both S(j) are done (they were,
+                    // before their P(j) reached this warp)
+                    if (!wait_all(&k_empty[st], (j / kTcStages) & 1)) break;
+                    load_k(j + 2, ids_ahead);
+                    k_loaded = j + 3;
+                }
             }
+            // direct K: the last two tiles' codes have landed before the CTA
+            // can exit (already so unless a wait above ran out; bounded)
+            for (int m = max(0, k_loaded - 2); m < k_loaded; ++m)
+                mbar_wait(smem_u32(&k_full[m % kTcStages]), (m / kTcStages) & 1, err);
         }
     } else {
         // ------------------------------------------------ softmax warps 0-15
@@ -551,7 +645,62 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const uint4* qp = reinterpret_cast<const uint4*>(
                 q + (static_cast<int64_t>(qs + pos_local) * n_q + head) * D);
             const uint32_t qbase = sbase + Ly::kOffQ + t * Ly::kQBytes;
-            if constexpr (std::is_same<T, QT>::value) {
+            if constexpr (kDirectK) {
+                // bf16 q -> two E4M3 parts: the row is scaled by 2^-e so that its
+                // largest magnitude lands in [128, 256), hi = e4m3(x) and lo =
+                // e4m3(x - hi) (exact for every element down to 2^-10 of the
+                // row's largest); 2^e goes into the row's softmax scale.  The
+                // pair meets to take the row's largest magnitude.
+                uint4 v[D / 16];
+                float amax = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) {
+                    v[cc] = valid ? __ldg(qp + hf * (D / 16) + cc) : make_uint4(0, 0, 0, 0);
+                    const uint32_t w4[4] = {v[cc].x, v[cc].y, v[cc].z, v[cc].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = Cvt<__nv_bfloat16>::unpack(w4[i]);
+                        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                }
+                xmax[1][t][hf][rr] = amax;   // (tile 1's slot: rewritten only after tile 0's meeting)
+                named_bar_sync(bar_id, 64);
+                const float rmax = fmaxf(amax, xmax[1][t][hf ^ 1][rr]);
+                int e = 0;
+                if (rmax > 0.f) {
+                    frexpf(rmax, &e);
+                    e = max(e - 8, -100);    // rmax * 2^-e in [128, 256) unless tiny
+                }
+                scale_log2 = ldexpf(scale_log2, e);
+                const float down = ldexpf(qsign ? -1.f : 1.f, -e);   // +-2^-e: the sign flip too
+                // 64 elements of the row: 4 chunks of 16 codes for each part
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {        // output word i: elements 4i .. 4i+3
+                        const uint4 src = v[2 * c4 + (i >> 1)];
+                        const uint32_t wa = (i & 1) ? src.z : src.x;
+                        const uint32_t wb = (i & 1) ? src.w : src.y;
+                        const float2 a = Cvt<__nv_bfloat16>::unpack(wa), b = Cvt<__nv_bfloat16>::unpack(wb);
+                        const float x0 = a.x * down, x1 = a.y * down, x2 = b.x * down, x3 = b.y * down;
+                        const uint32_t h01 = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+                        const uint32_t h23 = __nv_cvt_float2_to_fp8x2(make_float2(x2, x3), __NV_SATFINITE, __NV_E4M3);
+                        uint32_t d01, d23;
+                        widen4((h01 & 0xFFFFu) | (h23 << 16), d01, d23);   // hi values as fp16 pairs
+                        const float2 e01 = __half22float2(*reinterpret_cast<const __half2*>(&d01));
+                        const float2 e23 = __half22float2(*reinterpret_cast<const __half2*>(&d23));
+                        const uint32_t l01 = __nv_cvt_float2_to_fp8x2(make_float2(x0 - e01.x, x1 - e01.y), __NV_SATFINITE, __NV_E4M3);
+                        const uint32_t l23 = __nv_cvt_float2_to_fp8x2(make_float2(x2 - e23.x, x3 - e23.y), __NV_SATFINITE, __NV_E4M3);
+                        hw[i] = (h01 & 0xFFFFu) | (h23 << 16);
+                        lw[i] = (l01 & 0xFFFFu) | (l23 << 16);
+                    }
+                    const int c = hf * (D / 32) + c4;    // 16-byte chunk of the 128-byte row
+                    const uint32_t addr = qbase + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
+                    st_shared_v4(addr, hw[0], hw[1], hw[2], hw[3]);
+                    st_shared_v4(addr + Ly::kQLo, lw[0], lw[1], lw[2], lw[3]);
+                }
+            } else if constexpr (std::is_same<T, QT>::value) {
 #pragma unroll
                 for (int cc = 0; cc < D / 16; ++cc) {
                     const int c = hf * (D / 16) + cc;
@@ -790,7 +939,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 template <typename T, typename QT, int D, int BS, bool F8>
 static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl2)
 {
-    using Ly = PfLayout<T, D, F8>;
+    constexpr bool kBq = std::is_same<QT, __nv_bfloat16>::value;
+    using Ly = PfLayout<T, D, F8, kBq>;
     auto kern = prefill_tc_kernel<T, QT, D, BS, F8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -800,17 +950,22 @@ static cudaError_t run_prefill_tc(const PrefillArgs& a, cudaStream_t s, float sl
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap kmap{}, vmap{};
-    if constexpr (!F8) {   // (FP8 codes: plain bulk copies, the maps stay unused)
-        const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
+    const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * a.cache.n_kv_heads * BS;
+    if constexpr (!F8) {
         if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK ||
             encode_pool_map(&vmap, a.v_cache, a.cache.dtype, D, rows, 64, 16) != PA_OK)
+            return cudaErrorInvalidValue;
+    } else if constexpr (Ly::kDirectK) {
+        // K codes read by the score MMA: boxes of 16 rows x 128 codes, 128-byte
+        // swizzle (the other FP8 copies are plain bulk copies; vmap stays unused)
+        if (encode_pool_map(&kmap, a.k_cache, a.cache.dtype, D, rows, D, 16, 128) != PA_OK)
             return cudaErrorInvalidValue;
     }
     const int group = a.n_q / a.cache.n_kv_heads;
     const int64_t tiles = (static_cast<int64_t>(a.max_q) * group + kTcTiles * kTcRows - 1) /
                           (kTcTiles * kTcRows);
     dim3 grid(static_cast<unsigned>(tiles), a.cache.n_kv_heads, a.num_reqs);
-    kern<<<grid, PfWarps<F8>::kThreads, Ly::kDynBytes, s>>>(
+    kern<<<grid, PfWarps<F8, D, kBq>::kThreads, Ly::kDynBytes, s>>>(
         kmap, vmap, static_cast<const uint8_t*>(a.k_cache), static_cast<const uint8_t*>(a.v_cache),
         a.out, a.out_dtype, static_cast<const QT*>(a.q), a.block_tables, a.max_blocks,
         a.q_start, a.context_lens, a.max_q, a.n_q, a.cache.n_kv_heads, group, a.cache.num_blocks,
