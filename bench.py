@@ -50,8 +50,8 @@ NCU_TRAFFIC = {
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
 # chunks as the 60 GB pool): bytes per launch
 NCU_PREFILL_TRAFFIC = {
-    ("mixed-llama3-8b-bf16", "b13ead73ea0e5356"): (98299392 + 4567808, "compact pool, --set full"),
-    ("mixed-llama3-8b-fp8", "b13ead73ea0e5356"): (57555712 + 1308416, "compact pool, --set full"),
+    ("mixed-llama3-8b-bf16", "17aa5e07f1460786"): (98460416 + 5043456, "compact pool, --set full"),
+    ("mixed-llama3-8b-fp8", "17aa5e07f1460786"): (57560576 + 1417728, "compact pool, --set full"),
 }
 
 
