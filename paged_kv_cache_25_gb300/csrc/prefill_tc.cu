@@ -53,20 +53,21 @@ constexpr int kTcKeys = 128;      // keys per key tile
 constexpr int kTcStages = 2;      // K/V ring depth
 constexpr int kSoftmaxWarps = 8 * kTcTiles;   // two threads per row of each tile
 constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1;
-// FP8 pools: three warps widen codes into the rings.  In general a key tile
-// is 2 x (128 / kF8ChunkKeys) chunks (K's, then V's) and chunk g of the whole
-// sequence goes to converter g % 3.  With head_dim 128 and bf16 queries the
-// score MMA reads the K codes as they are (kind::f8f6f4; each q row, scaled by
-// a power of two, is exactly the sum of two E4M3 parts): the MMA warp loads
-// the codes by TMA a key tile ahead and the converters widen V alone.  (An
-// fp16 query has 11 significant bits, more than two E4M3 parts carry.)
+// FP8 pools: converter warps widen codes into the rings.  In general a key
+// tile is 2 x (128 / kF8ChunkKeys) chunks (K's, then V's) for three converters
+// and chunk g of the whole sequence goes to converter g % 3.  With head_dim 128
+// and bf16 queries the score MMA reads the K codes as they are (kind::f8f6f4;
+// each q row, scaled by a power of two, is exactly the sum of two E4M3 parts):
+// the MMA warp loads the codes by TMA a key tile ahead and two converters
+// widen V alone (three measured 2 % slower).  (An fp16 query has 11
+// significant bits, more than two E4M3 parts carry.)
 constexpr int kF8ChunkKeys = 32;   // keys per staged chunk of codes (16 or 32)
 constexpr int kF8MaxConverters = 3;
 constexpr int kF8MaxDepth = 2;     // staging buffers per converter
 template <bool F8, int D, bool BQ>
 struct PfMode {
     static constexpr bool kDirectK = F8 && D == 128 && BQ;   // K codes straight into the score MMA
-    static constexpr int kConverters = F8 ? 3 : 0;
+    static constexpr int kConverters = F8 ? (kDirectK ? 2 : 3) : 0;
     static constexpr int kDepth = 2;
 };
 // Warps after the softmax ones: the K and V producers (or the FP8
