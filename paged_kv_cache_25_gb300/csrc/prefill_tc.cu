@@ -68,15 +68,17 @@ template <bool F8, int D, bool BQ>
 struct PfMode {
     static constexpr bool kDirectK = F8 && D == 128 && BQ;   // K codes straight into the score MMA
     static constexpr int kConverters = F8 ? (kDirectK ? 2 : 3) : 0;
+    static constexpr int kKLoaders = kDirectK ? 1 : 0;   // direct K: a warp TMAs the K codes
     static constexpr int kDepth = 2;
 };
 // Warps after the softmax ones: the K and V producers (or the FP8
-// converters), then the MMA issuer.
+// converters, and with direct K the K-code loader), then the MMA issuer.
 template <bool F8, int D, bool BQ>
 struct PfWarps {
     using Mode = PfMode<F8, D, BQ>;
-    static constexpr int kProducers = F8 ? Mode::kConverters : 2;
+    static constexpr int kProducers = F8 ? Mode::kConverters + Mode::kKLoaders : 2;
     static constexpr int kFirstConverter = kSoftmaxWarps;
+    static constexpr int kKLoader = kFirstConverter + Mode::kConverters;   // (direct K only)
     static constexpr int kMma = kSoftmaxWarps + kProducers;
     static constexpr int kThreads = (kMma + 1) * 32;
     // the register file is split per SM sub-partition: 20 warps (5 on each)
@@ -276,7 +278,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t tmem = s_tmem;
 
     static_assert(!F8 || std::is_same<T, __half>::value, "FP8 codes widen to fp16 operands");
-    if (F8 && warp >= kFirstConv && warp < kMmaWarp) {
+    if (F8 && warp >= kFirstConv && warp < kFirstConv + Wp::Mode::kConverters) {
         // ------------------------------------------------ FP8 converters
         // Chunk g (tile g / kPerTile; K chunks first, then V) is widened by
         // converter g % kNc into its ring stage, which then gets
@@ -436,25 +438,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 request(n + kDepth);
             }
         }
-    } else if (!F8 && (warp == kKWarp || warp == kVWarp)) {
+    } else if ((!F8 && (warp == kKWarp || warp == kVWarp)) || (kDirectK && warp == Wp::kKLoader)) {
         // ------------------------------------------------ TMA producers
         // K and V have separate rings: K of key tile j is released once both
-        // S_t(j) are done, V of tile j once both P_t(j) V are.
+        // S_t(j) are done, V of tile j once both P_t(j) V are.  With direct K
+        // (FP8 pool) one warp loads the K codes: a tile is 8 boxes of 16 rows x
+        // 128 codes, 128-byte swizzled, as the score MMA reads them.
         if (lane == 0) {
-            const bool is_k = warp == kKWarp;
+            const bool is_k = F8 || warp == kKWarp;
             const CUtensorMap* map = is_k ? &kmap : &vmap;
             uint64_t* full_bar = is_k ? k_full : v_full;
             uint64_t* empty_bar = is_k ? k_empty : v_empty;
             const uint32_t ring_base = sbase + (is_k ? Ly::kOffK : Ly::kOffV);
+            const uint32_t tile_bytes = is_k ? Ly::kKBytes : Ly::kVBytes;
             prefetch_tensormap(map);
+            int loaded = 0;
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kTcStages;
                 if (j >= kTcStages &&
                     !mbar_wait(smem_u32(&empty_bar[st]), ((j / kTcStages) - 1) & 1, err))
                     break;
                 const uint32_t full = smem_u32(&full_bar[st]);
-                const uint32_t dst = ring_base + st * Ly::kKBytes;
-                mbar_arrive_expect_tx(full, Ly::kKBytes);
+                const uint32_t dst = ring_base + st * tile_bytes;
+                mbar_arrive_expect_tx(full, tile_bytes);
                 int b = 0;
 #pragma unroll
                 for (int c = 0; c < kTcKeys / 16; ++c) {
@@ -468,11 +474,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         }
                     }
                     const int row = (b * n_kv + kvh) * BS + (key0 % BS);
+                    if constexpr (F8) {
+                        tma_load_2d(dst + c * 2048, map, 0, row, full);
+                    } else {
 #pragma unroll
-                    for (int hx = 0; hx < Ly::kHalves; ++hx)
-                        tma_load_2d(dst + hx * (kTcKeys * 128) + c * 2048, map, hx * 64, row, full);
+                        for (int hx = 0; hx < Ly::kHalves; ++hx)
+                            tma_load_2d(dst + hx * (kTcKeys * 128) + c * 2048, map, hx * 64, row, full);
+                    }
                 }
+                loaded = j + 1;
             }
+            // the last two tiles' copies have landed before the warp can leave
+            // (already so unless a wait above ran out; bounded)
+            for (int m = max(0, loaded - kTcStages); m < loaded; ++m)
+                mbar_wait(smem_u32(&full_bar[m % kTcStages]), (m / kTcStages) & 1, err);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
@@ -538,45 +553,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, err));
             };
-            // Direct K (FP8 codes read by the score MMA): this warp loads key
-            // tile jt's codes into ring stage jt % 2, two tiles ahead of the
-            // scores that need them.  Lanes 0-7 look up the blocks of the tile's
-            // 16-key slabs a loop iteration early; lane 0 issues the boxes.
-            auto k_ids = [&](int jt) -> int {
-                if (!kDirectK || lane >= 8 || jt >= n_tiles) return 0;
-                // keys at or past L (masked in the softmax) read some block of the request
-                const int key = min(jt * kTcKeys + lane * 16, L - 1);
-                const int lb = key / BS;
-                return lb < max_blocks ? __ldg(block_tables + static_cast<int64_t>(r) * max_blocks + lb) : -1;
-            };
-            auto load_k = [&](int jt, int ids) {   // whole warp
-                int bb[kTcKeys / 16];
-#pragma unroll
-                for (int c = 0; c < kTcKeys / 16; ++c) bb[c] = __shfl_sync(0xffffffffu, ids, c);
-                if (lane == 0) {
-                    const uint32_t full = smem_u32(&k_full[jt % kTcStages]);
-                    const uint32_t dst = sbase + Ly::kOffK + (jt % kTcStages) * Ly::kKBytes;
-                    mbar_arrive_expect_tx(full, Ly::kKBytes);
-#pragma unroll
-                    for (int c = 0; c < kTcKeys / 16; ++c) {
-                        int b = bb[c];
-                        if (b < 0 || b >= num_blocks) {
-                            set_error(err, PA_ERR_OUT_OF_RANGE);
-                            b = 0;   // keep the ring moving; the outputs are flagged invalid
-                        }
-                        const int row = (b * n_kv + kvh) * BS + ((jt * kTcKeys + c * 16) % BS);
-                        tma_load_2d(dst + c * 2048, &kmap, 0, row, full);   // 16 rows x 128 codes
-                    }
-                }
-            };
-            int k_loaded = 0;   // direct K: key tiles requested so far
-            if constexpr (kDirectK) {
-                if (lane == 0) prefetch_tensormap(&kmap);
-                const int i0 = k_ids(0), i1 = k_ids(1);
-                load_k(0, i0);
-                if (n_tiles > 1) load_k(1, i1);
-                k_loaded = min(n_tiles, 2);
-            }
             bool ok = wait_all(&q_ready, 0) && wait_all(&k_full[0], 0);
             tc_fence_after();
             if (ok) {
@@ -587,7 +563,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % kTcStages, st1 = (j + 1) % kTcStages;
                 const bool more = j + 1 < n_tiles;
-                const int ids_ahead = k_ids(j + 2);   // direct K: blocks of tile j + 2
                 if (!wait_all(&v_full[st], (j / kTcStages) & 1)) break;
                 if (more && !wait_all(&k_full[st1], ((j + 1) / kTcStages) & 1)) break;
 #pragma unroll
@@ -604,18 +579,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if (!ok) break;
                 umma_commit_elect(smem_u32(&v_empty[st]));
                 if (more) umma_commit_elect(smem_u32(&k_empty[st1]));
-                if (kDirectK && j + 2 < n_tiles) {
-                    // stage st held K(j): free once both S(j) are done (they were,
-                    // before their P(j) reached this warp)
-                    if (!wait_all(&k_empty[st], (j / kTcStages) & 1)) break;
-                    load_k(j + 2, ids_ahead);
-                    k_loaded = j + 3;
-                }
             }
-            // direct K: the last two tiles' codes have landed before the CTA
-            // can exit (already so unless a wait above ran out; bounded)
-            for (int m = max(0, k_loaded - 2); m < k_loaded; ++m)
-                mbar_wait(smem_u32(&k_full[m % kTcStages]), (m / kTcStages) & 1, err);
         }
     } else {
         // ------------------------------------------------ softmax warps 0-15
