@@ -10,13 +10,14 @@
 // one stream of K/V.  The M rows are (position, head) pairs of one GQA group,
 // position-major, so one pass over the keys serves all the query heads that
 // share the KV head.  Keys go in tiles of 128.
-//   warps 8, 9: TMA producers: 16-row K (warp 8) and V (warp 9) slabs of each
-//             128-key tile into their own 2-stage rings (128-byte swizzle), one
-//             block-table lookup per block;
-//   warp 10 : one thread issues the MMAs: S_t = Q_t K^T (M 128, N 128, K = d)
-//             into TMEM, O_t += P_t V (M 128, N = d, K 128) into TMEM, in the
-//             order P_A(j) V, S_A(j+1), P_B(j) V, S_B(j+1): while one tile's rows
-//             run their softmax the tensor cores work on the other tile;
+//   warps 16, 17: TMA producers: 16-row K (warp 16) and V (warp 17) slabs of
+//             each 128-key tile into their own 2-stage rings (128-byte swizzle),
+//             one block-table lookup per block (FP8 pools: see below);
+//   last warp: the MMA issuer, a warp-wide loop in which one elected lane
+//             issues S_t = Q_t K^T (M 128, N 128, K = d) into TMEM and
+//             O_t += P_t V (M 128, N = d, K 128) into TMEM, in the order
+//             P_A(j) V, S_A(j+1), P_B(j) V, S_B(j+1): while one tile's rows run
+//             their softmax the tensor cores work on the other tile;
 //   warps 0-15: two threads per M row of a tile (warps 0-3 and 8-11 tile A,
 //             4-7 and 12-15 tile B), each with 64 of a key tile's 128 keys and
 //             half of O's columns; the pair swaps partial row maxima through
@@ -28,11 +29,13 @@
 //             halves with bf16 operands (P V keeps ~16 bits of P), as one fp16
 //             part with fp16 operands (11 bits); the P V MMA takes P straight
 //             from TMEM.  At the end O / l goes to global memory.
-// FP8 (E4M3) pools: three converter warps replace the two producers; they copy
-// the codes chunk by chunk into staging buffers and widen them exactly to fp16
-// in the same rings (V kept in the pool's transposed [d][keys] pieces, a
-// K-major operand of P V); keys at or past the context are written as zeros.  The
-// MMAs run on fp16 operands (bf16 queries are scaled into fp16 per row).
+// FP8 (E4M3) pools: converter warps replace the two producers; they copy the
+// codes chunk by chunk into staging buffers and widen them exactly to fp16 in
+// the same rings (V kept in the pool's transposed [d][keys] pieces, a K-major
+// operand of P V); keys at or past the context are written as zeros.  The
+// MMAs run on fp16 operands (bf16 queries are scaled into fp16 per row), except
+// that with head_dim 128 and bf16 queries the score MMAs read the K codes
+// themselves (a K-loader warp TMAs them; two converters widen V alone).
 // k_scale is folded into the softmax scale and v_scale into the output.
 // All waits are bounded; the kernel never traps.
 #include <cuda_fp8.h>
