@@ -50,8 +50,8 @@ NCU_TRAFFIC = {
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
 # chunks as the 60 GB pool): bytes per launch
 NCU_PREFILL_TRAFFIC = {
-    ("mixed-llama3-8b-bf16", "17aa5e07f1460786"): (98460416 + 5043456, "compact pool, --set full"),
-    ("mixed-llama3-8b-fp8", "17aa5e07f1460786"): (57560576 + 1417728, "compact pool, --set full"),
+    ("mixed-llama3-8b-bf16", "5b0f802bd3d8b04e"): (98457600 + 4648704, "compact pool, --set full"),
+    ("mixed-llama3-8b-fp8", "5b0f802bd3d8b04e"): (57556224 + 1413632, "compact pool, --set full"),
 }
 
 
