@@ -45,8 +45,8 @@ namespace pa {
 
 constexpr int kDecWarps = 4;
 constexpr int kRows = 16;            // K/V rows per pipeline stage
-constexpr int kMaxPartBlocks = 64;   // blocks per partition (part_tokens / block_size)
-constexpr int kPrefixCap = 2048;     // sequences whose partition prefix sum fits in smem
+constexpr int kMaxPartBlocks = 128;   // blocks per partition (part_tokens / block_size)
+constexpr int kPrefixCap = 1024;      // sequences whose partition prefix sum fits in smem
 
 __device__ __forceinline__ void store_any(void* out, int64_t idx, float v, pa_dtype dt)
 {
@@ -67,8 +67,9 @@ constexpr int decode_ctas_per_sm(bool fp8, int D = 128, int RU = 8)
     return RU == 4 ? 4 : (fp8 || (D == 64 && RU == 8) ? 3 : 2);
 }
 constexpr int kSmemPerSm = 233472;    // 228 KB of shared memory per SM
-// bound on the kernel's static shared memory (ptxas: 9,296 B at d 128 with a
-// 2-stage ring, 9,424 B at d 64 with 6 stages; the prefix table is 8 KB of it)
+// bound on the kernel's static shared memory (ptxas: 5,712-5,936 B, of which the
+// prefix table is 4 KB; the bound is kept at its earlier value, so the ring
+// depths stay those measured)
 constexpr int kStaticSmem = 9728;
 constexpr int kPreferSepRed = 1;      // give the combine its own buffer when it fits
 constexpr int kStaticUnitsPerCta = 4; // batches up to this many units per CTA: round robin

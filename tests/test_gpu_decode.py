@@ -133,7 +133,7 @@ def test_decode_1024_token_partitions_all_outputs():
 
 
 def test_decode_more_sequences_than_the_prefix_table():
-    """2,100 sequences (past the 2,048 whose partition prefix sums fit in shared
+    """2,100 sequences (past the 1,024 whose partition prefix sums fit in shared
     memory): units are numbered per (sequence, partition index) instead; every
     output checked, lengths spanning one to several partitions."""
     rng = np.random.default_rng(55)
