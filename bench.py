@@ -42,9 +42,9 @@ FALLBACK_HBM_GBS = 6800.0
 # K/V bytes of the captured launch, what was captured); a record of another
 # batch of the same workload is scaled by its unique K/V bytes.
 NCU_TRAFFIC = {
-    ("llama3-8b-bf16", "63f47179fb67718c"): (2371995136 + 13369600, 2359717888,
+    ("llama3-8b-bf16", "bcc6fa94f0d99065"): (2371989760 + 13039872, 2359717888,
                                              "full 256-sequence batch, one-pass capture"),
-    ("llama3-8b-fp8", "63f47179fb67718c"): (1188201216 + 12453888, 1179858944,
+    ("llama3-8b-fp8", "bcc6fa94f0d99065"): (1188177920 + 12422400, 1179858944,
                                             "full 256-sequence batch, one-pass capture"),
 }
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
