@@ -61,7 +61,7 @@ constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1;
 // and chunk g of the whole sequence goes to converter g % 3.  With head_dim 128
 // and bf16 queries the score MMA reads the K codes as they are (kind::f8f6f4;
 // each q row, scaled by a power of two, is exactly the sum of two E4M3 parts):
-// the MMA warp loads the codes by TMA a key tile ahead and two converters
+// a loader warp of its own TMAs the codes into the K ring and two converters
 // widen V alone (three measured 2 % slower).  (An fp16 query has 11
 // significant bits, more than two E4M3 parts carry.)
 constexpr int kF8ChunkKeys = 32;   // keys per staged chunk of codes (16 or 32)
