@@ -29,8 +29,14 @@
 //     of P (rows 8-15 would otherwise be padding).  Groups of more than 8 heads
 //     are handled as several 8-head sub-groups.
 // Multi-query instantiations (MQ) take q_per_seq query rows per sequence: the
-// rows of a KV head are (head, query) pairs, head-major, 8 per sub-group, and
-// query i of q_per_seq sees the keys up to L - q_per_seq + i.
+// rows of a KV head are (head, query) pairs, head-major, 8 per sub-group (16
+// per unit when a KV head has more than 8), and query i of q_per_seq sees the
+// keys up to L - q_per_seq + i.
+// FP8 pools: a stage's K codes arrive by TMA and its V piece (stored
+// transposed, 16 tokens x head_dim) by one 1-D bulk copy; fragments are
+// widened to fp16 in registers.  With at most 4 query heads a KV head the
+// FP8 decode runs transposed (4-row units, RU 4): the stage's 16 tokens are
+// the MMA rows, see kTr below.
 #include <cuda_fp8.h>
 
 #include "pa_device.cuh"
