@@ -42,16 +42,16 @@ FALLBACK_HBM_GBS = 6800.0
 # K/V bytes of the captured launch, what was captured); a record of another
 # batch of the same workload is scaled by its unique K/V bytes.
 NCU_TRAFFIC = {
-    ("llama3-8b-bf16", "bcc6fa94f0d99065"): (2371989760 + 13039872, 2359717888,
+    ("llama3-8b-bf16", "457fd1bedd821cbf"): (2371978496 + 13387776, 2359717888,
                                              "full 256-sequence batch, one-pass capture"),
-    ("llama3-8b-fp8", "bcc6fa94f0d99065"): (1188177920 + 12422400, 1179858944,
+    ("llama3-8b-fp8", "457fd1bedd821cbf"): (1188195584 + 12364544, 1179858944,
                                             "full 256-sequence batch, one-pass capture"),
 }
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
 # chunks as the 60 GB pool): bytes per launch
 NCU_PREFILL_TRAFFIC = {
-    ("mixed-llama3-8b-bf16", "5b0f802bd3d8b04e"): (98457600 + 4648704, "compact pool, --set full"),
-    ("mixed-llama3-8b-fp8", "5b0f802bd3d8b04e"): (57556224 + 1413632, "compact pool, --set full"),
+    ("mixed-llama3-8b-bf16", "73db632eac0b9797"): (98445824 + 4631552, "compact pool, --set full"),
+    ("mixed-llama3-8b-fp8", "73db632eac0b9797"): (57555968 + 1261056, "compact pool, --set full"),
 }
 
 
