@@ -42,9 +42,9 @@ FALLBACK_HBM_GBS = 6800.0
 # K/V bytes of the captured launch, what was captured); a record of another
 # batch of the same workload is scaled by its unique K/V bytes.
 NCU_TRAFFIC = {
-    ("llama3-8b-bf16", "457fd1bedd821cbf"): (2371978496 + 13387776, 2359717888,
+    ("llama3-8b-bf16", "156a5e1d9ddf2e4e"): (2371995904 + 13372672, 2359717888,
                                              "full 256-sequence batch, one-pass capture"),
-    ("llama3-8b-fp8", "457fd1bedd821cbf"): (1188195584 + 12364544, 1179858944,
+    ("llama3-8b-fp8", "156a5e1d9ddf2e4e"): (1188186112 + 12436224, 1179858944,
                                             "full 256-sequence batch, one-pass capture"),
 }
 # chunked prefill of the mixed step (the compact-pool capture runs the same four

@@ -74,9 +74,8 @@ constexpr int decode_ctas_per_sm(bool fp8, int D = 128, int RU = 8)
 }
 constexpr int kSmemPerSm = 233472;    // 228 KB of shared memory per SM
 // bound on the kernel's static shared memory (ptxas: 5,712-5,936 B, of which the
-// prefix table is 4 KB; the bound is kept at its earlier value, so the ring
-// depths stay those measured)
-constexpr int kStaticSmem = 9728;
+// prefix table is 4 KB)
+constexpr int kStaticSmem = 6144;
 constexpr int kPreferSepRed = 1;      // give the combine its own buffer when it fits
 constexpr int kStaticUnitsPerCta = 4; // batches up to this many units per CTA: round robin
 
@@ -88,17 +87,18 @@ constexpr int decode_dyn_avail(bool fp8, int D = 128, int RU = 8)
 }
 
 // Ring depth per warp: about `budget` bytes of K+V in flight per warp, at least
-// 2 stages; when a separate combine buffer fits beside a ring of at least 2
-// stages, the ring is cut to what fits beside it.
+// 2 stages, and no more than the dynamic shared memory holds.  Depth comes
+// before a separate combine buffer: when the two do not fit together, the
+// combine aliases the (then idle) rings.
 template <typename T, int D, bool FP8, int RU = 8>
 constexpr int decode_stages()
 {
     constexpr int stage = 2 * kRows * D * (FP8 ? 1 : static_cast<int>(sizeof(T)));
     constexpr int budget = FP8 ? 12288 : 24576;
     constexpr int ns = budget / stage > 2 ? budget / stage : 2;
-    constexpr int red = kDecWarps * RU * (D + 2) * 4;
-    constexpr int fit = (decode_dyn_avail(FP8, D, RU) - red) / (kDecWarps * stage);
-    return kPreferSepRed && fit >= 2 ? (fit < ns ? fit : ns) : ns;
+    constexpr int cap = (decode_dyn_avail(FP8, D, RU) - 1024) / (kDecWarps * stage);
+    static_assert(cap >= 2, "a ring of two stages per warp must fit");
+    return ns < cap ? ns : cap;
 }
 
 // FP8 pools: a stage holds 16 rows of E4M3 K codes (swizzled rows of D bytes)
