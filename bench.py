@@ -50,8 +50,8 @@ NCU_TRAFFIC = {
 # chunked prefill of the mixed step (the compact-pool capture runs the same four
 # chunks as the 60 GB pool): bytes per launch
 NCU_PREFILL_TRAFFIC = {
-    ("mixed-llama3-8b-bf16", "73db632eac0b9797"): (98445824 + 4631552, "compact pool, --set full"),
-    ("mixed-llama3-8b-fp8", "73db632eac0b9797"): (57555968 + 1261056, "compact pool, --set full"),
+    ("mixed-llama3-8b-bf16", "32cbb231cfdc1f9a"): (98471424 + 4715776, "compact pool, --set full"),
+    ("mixed-llama3-8b-fp8", "32cbb231cfdc1f9a"): (57562624 + 1404672, "compact pool, --set full"),
 }
 
 

@@ -50,10 +50,69 @@
 
 namespace pa {
 
+// Four MMAs into one accumulator from a converged warp, under one election:
+// D (+)= A_i B_i for i = 0..3 in that order, the first accumulating only if
+// `acc`, the others always.  Next to the busy softmax warps the issuing warp
+// gets few issue slots, so fewer instructions per MMA issue faster.
+// A and B from shared memory (kind::f16, or kind::f8f6f4 with E4M3 codes):
+template <bool kF8>
+__device__ __forceinline__ void umma4_ss(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1, uint64_t b1,
+                                         uint64_t a2, uint64_t b2, uint64_t a3, uint64_t b3,
+                                         uint32_t idesc, uint32_t acc)
+{
+    if constexpr (kF8) {
+        asm volatile(
+            "{\n\t.reg .pred e, p, q;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %10, 0;\n\t"
+            "setp.eq.b32 q, %9, %9;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %9, p;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %6, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %7, %8, %9, q;\n\t}" ::"r"(d),
+            "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc),
+            "r"(acc)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred e, p, q;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %10, 0;\n\t"
+            "setp.eq.b32 q, %9, %9;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %9, p;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %9, q;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %9, q;\n\t}" ::"r"(d),
+            "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc),
+            "r"(acc)
+            : "memory");
+    }
+}
+
+// the same with A from tensor memory (kind::f16)
+__device__ __forceinline__ void umma4_ts(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1, uint64_t b1,
+                                         uint32_t a2, uint64_t b2, uint32_t a3, uint64_t b3,
+                                         uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, p, q;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 q, %9, %9;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %9, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %9, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %9, q;\n\t}" ::"r"(d),
+        "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(idesc),
+        "r"(acc)
+        : "memory");
+}
+
 constexpr int kTcRows = 128;      // M rows per tile
 constexpr int kTcTiles = 2;       // tiles per CTA (A, B)
 constexpr int kTcKeys = 128;      // keys per key tile
 constexpr int kTcStages = 2;      // K/V ring depth
+constexpr int kRankedReqs = 64;   // requests ordered by context length, at most
 constexpr int kSoftmaxWarps = 8 * kTcTiles;   // two threads per row of each tile
 constexpr int kKWarp = kSoftmaxWarps, kVWarp = kSoftmaxWarps + 1;
 // FP8 pools: converter warps widen codes into the rings.  In general a key
@@ -205,9 +264,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     constexpr uint32_t kIdescPV = idesc_f16(kBf16, false, !F8, kTcRows, D);
     static_assert(BS % 16 == 0 && kTcKeys % BS == 0, "block size must divide the key tile");
 
-    // blocks with more keys first: the last position blocks are the heaviest
+    // heavier CTAs first, as the grid is scheduled in index order: the z index
+    // is the request's rank by context length (longest first, ties by index;
+    // up to kRankedReqs requests, else request order), and within a request
+    // the last position blocks, which see the most keys, come first
+    static_assert(kRankedReqs <= Wp::kThreads, "one thread per ranked request");
+    int r = blockIdx.z;
+    if (gridDim.z > 1 && gridDim.z <= kRankedReqs) {
+        __shared__ int s_req;
+        const int R = gridDim.z, i = threadIdx.x;
+        if (i < R) {
+            const int Li = __ldg(context_lens + i);
+            int rank = 0;
+            for (int k = 0; k < R; ++k) {
+                const int Lk = __ldg(context_lens + k);
+                rank += (Lk > Li || (Lk == Li && k < i)) ? 1 : 0;
+            }
+            if (rank == static_cast<int>(blockIdx.z)) s_req = i;
+        }
+        __syncthreads();
+        r = s_req;
+    }
     const int blk = gridDim.x - 1 - blockIdx.x;
-    const int kvh = blockIdx.y, r = blockIdx.z;
+    const int kvh = blockIdx.y;
     const int qs = __ldg(q_start + r);
     const int C = __ldg(q_start + r + 1) - qs;
     const int L = __ldg(context_lens + r);
@@ -222,7 +301,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         return;
     }
     const int ctx0 = L - C;
-    // key tiles each tile's rows need (0: the tile has no rows); n_t[0] <= n_t[1]
+    // key tiles each tile's rows need (0: the tile has no rows); when both
+    // tiles have rows, n_t[0] <= n_t[1]
     int n_t[kTcTiles];
 #pragma unroll
     for (int t = 0; t < kTcTiles; ++t) {
@@ -455,26 +535,41 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const uint32_t ring_base = sbase + (is_k ? Ly::kOffK : Ly::kOffV);
             const uint32_t tile_bytes = is_k ? Ly::kKBytes : Ly::kVBytes;
             prefetch_tensormap(map);
+            // block ids of the 16-key pieces of a tile, read a tile ahead: eight
+            // independent loads whose latency the wait for a free stage hides
+            // (read next to each copy they would be serial, the copies being
+            // ordered after them)
+            constexpr int kPieces = kTcKeys / 16;
+            const int32_t* table = block_tables + static_cast<int64_t>(r) * max_blocks;
+            auto tile_ids = [&](int j, int (&ids)[kPieces]) {
+#pragma unroll
+                for (int c = 0; c < kPieces; ++c) {
+                    const int key0 = j * kTcKeys + c * 16;
+                    const int lb = key0 / BS;
+                    // past L the tile's rows are masked: reuse the last block
+                    ids[c] = (j >= n_tiles || key0 >= L) ? (c > 0 ? ids[c - 1] : 0)
+                                                          : (lb < max_blocks ? __ldg(table + lb) : -1);
+                }
+            };
+            int ids[kPieces], ids_next[kPieces];
+            tile_ids(0, ids);
             int loaded = 0;
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kTcStages;
+                tile_ids(j + 1, ids_next);
                 if (j >= kTcStages &&
                     !mbar_wait(smem_u32(&empty_bar[st]), ((j / kTcStages) - 1) & 1, err))
                     break;
                 const uint32_t full = smem_u32(&full_bar[st]);
                 const uint32_t dst = ring_base + st * tile_bytes;
                 mbar_arrive_expect_tx(full, tile_bytes);
-                int b = 0;
 #pragma unroll
-                for (int c = 0; c < kTcKeys / 16; ++c) {
+                for (int c = 0; c < kPieces; ++c) {
                     const int key0 = j * kTcKeys + c * 16;
-                    if (key0 < L) {   // past L the tile's rows are masked: reuse the last block
-                        const int lb = key0 / BS;
-                        b = lb < max_blocks ? __ldg(block_tables + static_cast<int64_t>(r) * max_blocks + lb) : -1;
-                        if (b < 0 || b >= num_blocks) {
-                            set_error(err, PA_ERR_OUT_OF_RANGE);
-                            b = 0;   // keep the ring moving; the outputs are flagged invalid
-                        }
+                    int b = ids[c];
+                    if (b < 0 || b >= num_blocks) {
+                        set_error(err, PA_ERR_OUT_OF_RANGE);
+                        b = 0;   // keep the ring moving; the outputs are flagged invalid
                     }
                     const int row = (b * n_kv + kvh) * BS + (key0 % BS);
                     if constexpr (F8) {
@@ -486,6 +581,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     }
                 }
                 loaded = j + 1;
+#pragma unroll
+                for (int c = 0; c < kPieces; ++c) ids[c] = ids_next[c];
             }
             // the last two tiles' copies have landed before the warp can leave
             // (already so unless a wait above ran out; bounded)
@@ -516,18 +613,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if constexpr (kDirectK) {
                     // E4M3 x E4M3: 32 codes (32 bytes) per k-step of the one
                     // 128-byte row; q's hi part, then its lo part, into S
+                    static_assert(D == 128, "four k-steps of 32 codes");
 #pragma unroll
-                    for (int kk = 0; kk < D / 32; ++kk) {
-                        umma_f8_elect(d_s, dqt + kk * 2, dks + kk * 2, kIdescQK8, kk > 0 ? 1u : 0u);
-                        umma_f8_elect(d_s, dqt + kQLo + kk * 2, dks + kk * 2, kIdescQK8, 1u);
-                    }
+                    for (int kk = 0; kk < D / 32; kk += 2)
+                        umma4_ss<true>(d_s, dqt + kk * 2, dks + kk * 2, dqt + kQLo + kk * 2, dks + kk * 2,
+                                       dqt + (kk + 1) * 2, dks + (kk + 1) * 2,
+                                       dqt + kQLo + (kk + 1) * 2, dks + (kk + 1) * 2, kIdescQK8,
+                                       kk > 0 ? 1u : 0u);
                 } else {
+                    // 32 bytes per k-step; 4 k-steps per 64-element half
+                    auto oq = [&](int kk) { return static_cast<uint32_t>((kk >> 2) * kQHalf + (kk & 3) * 2); };
+                    auto ok_ = [&](int kk) { return static_cast<uint32_t>((kk >> 2) * kKHalf + (kk & 3) * 2); };
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off_q = (kk >> 2) * kQHalf + (kk & 3) * 2;   // 32 bytes per k-step
-                        const uint32_t off_k = (kk >> 2) * kKHalf + (kk & 3) * 2;
-                        umma_f16_elect(d_s, dqt + off_q, dks + off_k, kIdescQK, kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < D / 16; kk += 4)
+                        umma4_ss<false>(d_s, dqt + oq(kk), dks + ok_(kk), dqt + oq(kk + 1), dks + ok_(kk + 1),
+                                        dqt + oq(kk + 2), dks + ok_(kk + 2), dqt + oq(kk + 3),
+                                        dks + ok_(kk + 3), kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 umma_commit_elect(smem_u32(&s_full[t]));
             };
@@ -537,20 +638,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 const uint64_t dvs = dv + st * kVStage;
                 const uint32_t d_o = tmem + Ly::kTmemO + t * D;
                 const uint32_t a_p = tmem + Ly::kTmemS + t * 128;
+                // keys 16 ks .. +15: 32-key chunk ks / 2 holds hi in its first
+                // 16 columns and lo in the next 16 (16 keys = 8 columns)
+                auto col = [&](int ks) { return static_cast<uint32_t>((ks >> 1) * 32 + (ks & 1) * 8); };
+                // V rows of these 16 keys: 16 rows of 128 B (MN-major), or
+                // 32 B into a 64-key half of the [d][keys] tile (K-major)
+                auto vst = [&](int ks) {
+                    return static_cast<uint32_t>(F8 ? (ks >> 2) * ((D * 128) >> 4) + (ks & 3) * 2
+                                                    : ks * (2048 >> 4));
+                };
+                if constexpr (kOneP) {
 #pragma unroll
-                for (int ks = 0; ks < kTcKeys / 16; ++ks) {
-                    // keys 16 ks .. +15: 32-key chunk ks / 2 holds hi in its first
-                    // 16 columns and lo in the next 16 (16 keys = 8 columns)
-                    const uint32_t col = (ks >> 1) * 32 + (ks & 1) * 8;
-                    // V rows of these 16 keys: 16 rows of 128 B (MN-major), or
-                    // 32 B into a 64-key half of the [d][keys] tile (K-major)
-                    const uint32_t vst = F8 ? (ks >> 2) * ((D * 128) >> 4) + (ks & 3) * 2
-                                            : ks * (2048 >> 4);
-                    umma_f16_ts_elect(d_o, a_p + col, dvs + vst, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-                    if constexpr (!kOneP)   // bf16 operands: P's lo part too
-                        umma_f16_ts_elect(d_o, a_p + col + 16, dvs + vst, kIdescPV, 1u);
+                    for (int ks = 0; ks < kTcKeys / 16; ks += 4)
+                        umma4_ts(d_o, a_p + col(ks), dvs + vst(ks), a_p + col(ks + 1), dvs + vst(ks + 1),
+                                 a_p + col(ks + 2), dvs + vst(ks + 2), a_p + col(ks + 3), dvs + vst(ks + 3),
+                                 kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+                } else {   // bf16 operands: P's hi part, then its lo part, per 16 keys
+#pragma unroll
+                    for (int ks = 0; ks < kTcKeys / 16; ks += 2)
+                        umma4_ts(d_o, a_p + col(ks), dvs + vst(ks), a_p + col(ks) + 16, dvs + vst(ks),
+                                 a_p + col(ks + 1), dvs + vst(ks + 1), a_p + col(ks + 1) + 16,
+                                 dvs + vst(ks + 1), kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
                 }
-                umma_commit_elect(smem_u32(&pv_done[t]));
+                if (j + 1 == n_t[t]) umma_commit_elect(smem_u32(&pv_done[t]));   // O_t complete
             };
             // every lane polls; the warp goes on only if all saw the phase
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
@@ -563,11 +673,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     if (n_t[t] > 0) issue_qk(t, 0);
                 umma_commit_elect(smem_u32(&k_empty[0]));
             }
+            ok = ok && (n_tiles == 0 || wait_all(&v_full[0], 0));
+            // Per key tile j: each tile's P_t(j) V, then its S_t(j + 1).  The
+            // waits for the next key tile's K and V sit after a P V, while its
+            // MMAs are still queued, so the tensor pipe does not run dry while
+            // this warp waits; only the P waits lie on the pipeline's path.
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % kTcStages, st1 = (j + 1) % kTcStages;
                 const bool more = j + 1 < n_tiles;
-                if (!wait_all(&v_full[st], (j / kTcStages) & 1)) break;
-                if (more && !wait_all(&k_full[st1], ((j + 1) / kTcStages) & 1)) break;
+                const int last_t = j < n_t[1] ? 1 : 0;   // the last tile with key tile j
+                bool k_next = false;                      // K(j + 1) has landed
 #pragma unroll
                 for (int t = 0; t < kTcTiles; ++t) {
                     if (j >= n_t[t]) continue;
@@ -577,11 +692,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     }
                     tc_fence_after();
                     issue_pv(t, j);
-                    if (j + 1 < n_t[t]) issue_qk(t, j + 1);
+                    if (t == last_t) umma_commit_elect(smem_u32(&v_empty[st]));   // V(j) read
+                    const bool qk = j + 1 < n_t[t];
+                    if (qk || (t == last_t && more)) {
+                        if (!k_next && !wait_all(&k_full[st1], ((j + 1) / kTcStages) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        k_next = true;
+                        if (t == last_t && !wait_all(&v_full[st1], ((j + 1) / kTcStages) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    if (qk) issue_qk(t, j + 1);
                 }
                 if (!ok) break;
-                umma_commit_elect(smem_u32(&v_empty[st]));
-                if (more) umma_commit_elect(smem_u32(&k_empty[st1]));
+                if (more) umma_commit_elect(smem_u32(&k_empty[st1]));   // K(j + 1) read
             }
         }
     } else {
@@ -879,7 +1007,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const float lsum = l + xsum[t][hf ^ 1][rr];
             stop = stop || xstop_end[t][hf ^ 1][rr] != 0;
             const bool ok = !__any_sync(0xffffffffu, stop) &&
-                            mbar_wait(smem_u32(&pv_done[t]), (nt - 1) & 1, err);
+                            mbar_wait(smem_u32(&pv_done[t]), 0, err);
             if (__all_sync(0xffffffffu, ok)) {
                 tc_fence_after();
                 const float inv = (F8 ? v_scale : 1.f) / lsum;
