@@ -61,6 +61,12 @@ CASES = [
     (3, [(500, 64), (0, 16), (16, 16)], 8, 1, 64, 32, torch.float16),     # MQA g=8
     (4, [(1000, 130)], 40, 40, 128, 16, torch.float16),                   # MHA
     (5, [(47, 200), (1, 3)], 12, 4, 128, 32, torch.bfloat16),             # g=3, rows straddle
+    # CTAs go longest request first: equal context lengths (ties by index)
+    (6, [(100, 20), (290, 50), (100, 20), (0, 120), (339, 1)], 8, 2, 128, 16, torch.bfloat16),
+    # more requests than the kernel ranks (64): call order
+    (7, [(int(c), int(n)) for c, n in zip(np.random.default_rng(7).integers(0, 60, 70),
+                                          np.random.default_rng(8).integers(1, 10, 70))],
+     4, 2, 64, 16, torch.float16),
 ]
 
 
