@@ -185,3 +185,22 @@ def test_prefill_fp8_host_validation():
     assert call(pa._Desc(64, 16, 8, 96, fp8, 0.5, 0.5, pa.PA_BF16)) == pa.PA_ERR_UNSUPPORTED
     assert "FP8" in pa.lib().pa_last_error_message().decode() or \
         "head_dim" in pa.lib().pa_last_error_message().decode()
+
+
+def test_stored_dram_traffic_matches_the_kernel_sources():
+    """The bench reports ncu DRAM bytes only for the kernel sources they were
+    captured on (keyed by a hash of those sources): the headline and FP8
+    decode batches and both mixed steps' prefills have a capture of the
+    sources as they stand, and each capture is at least the unique bytes."""
+    import importlib.util
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    dh = bench._src_hash(bench.DECODE_SOURCES)
+    ph = bench._src_hash(bench.PREFILL_SOURCES)
+    for name in ("llama3-8b-bf16", "llama3-8b-fp8"):
+        traffic, unique = bench.NCU_TRAFFIC[(name, dh)][:2]
+        assert unique <= traffic <= 1.05 * unique
+    for name in ("mixed-llama3-8b-bf16", "mixed-llama3-8b-fp8"):
+        assert (name, ph) in bench.NCU_PREFILL_TRAFFIC
